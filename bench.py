@@ -1,0 +1,492 @@
+#!/usr/bin/env python
+"""Benchmark: sparse shared-KV MLA attention, CSA decode, one GB300 per rank.
+
+A step is one pass of the whole hot path over one batch: the device planner
+(sfm_metadata) and the attention + split combine (sfm_forward) for B = 32
+decode query rows of q_n = 64 heads, each attending a 128-row window of its
+paged ori cache plus 512 top-k compressed rows (cmp_ratio 4).  Inputs are
+synthetic (seeded), resident in HBM, and rotate over enough independent input
+sets that the attended bytes of consecutive steps never sit in L2.
+
+Metric: attended KV rows per second (each attended row counted once per query
+row, not per head), reported with TFLOP/s and the roofline of the dominant
+kernel.  ``e2e`` repeats the measurement through the public two-call API with
+the step's inputs copied from pinned host memory and O / LSE read back.
+
+``--impl reference`` times the CPU oracle (fp64, all host cores) on the same
+workload instead; it is a deliberately slow correctness reference, not a
+competitor.
+
+Multi-GPU: the path has no exchange step, so N ranks run N independent
+replicas (weak scaling); the time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import glob
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+WORKLOADS = ("csa_decode", "hca_decode", "packed_decode")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", choices=WORKLOADS, default="csa_decode")
+    ap.add_argument("--sets", type=int, default=16, help="rotating input sets (defeats L2)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (replicas only)
+# ---------------------------------------------------------------------------
+def dist_init(backend):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.lines = []
+        self.t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu_id, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+        time.sleep(0.3)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self):
+        return time.time()
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0=None, t1=None):
+        rows = []
+        for ts, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                rows.append((ts, float(parts[0]), float(parts[1]), parts[3:]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"], "samples": 0}
+        inside = [r for r in rows if (t0 is None or r[0] >= t0) and (t1 is None or r[0] <= t1)]
+        window = "timed region"
+        if not inside:
+            inside, window = rows, "warm-up + timed region"
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in inside:
+            flags = r[3][1:]
+            for n, f in zip(names, flags):
+                if f.strip().lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(r[1] for r in inside), "sm_max_mhz": max(r[2] for r in inside),
+                "reasons": sorted(reasons), "samples": len(inside), "window": window}
+
+
+# ---------------------------------------------------------------------------
+# workload accounting (algorithmic bytes / FLOPs)
+# ---------------------------------------------------------------------------
+def make_problem(workload, device, seed):
+    import sfm_inputs as S
+    return S.WORKLOADS[workload](device=device, seed=seed)
+
+
+def accounting(prob, sfm):
+    """Attended rows, algorithmic HBM bytes and FLOPs of one pass over the batch."""
+    params = sfm.make_params(**prob.attrs())
+    tens = sfm.make_tensors(prob.t["q"], prob.t["ori_kv"], **prob.tensor_kwargs())
+    cap = (prob.ori_topk or (prob.ori_win_left + prob.ori_win_right + 1)) + (prob.cmp_topk or prob.max_seqlen_cmp_kv)
+    dev = prob.t["q"].device
+    rows = torch.full((prob.num_tokens, cap), -1, dtype=torch.int32, device=dev)
+    counts = torch.zeros(prob.num_tokens, dtype=torch.int32, device=dev)
+    sfm.sfm_debug_attended(params, tens, rows, cap, counts)
+    torch.cuda.synchronize()
+    valid = rows >= 0
+    attended = int(valid.sum().item())
+    # block-table entries touched: distinct (row, source, block) per query row
+    bt_entries = 0
+    if prob.layout_kv == "PAGED":
+        src = (rows >> 30) & 1
+        pos = rows & 0x3FFFFFFF
+        for s, bs in ((0, prob.ori_block_size), (1, prob.cmp_block_size)):
+            if bs <= 0:
+                continue
+            m = valid & (src == s)
+            blk = torch.where(m, pos // bs, torch.full_like(pos, -1))
+            srt, _ = torch.sort(blk, dim=1)
+            new = (srt[:, 1:] != srt[:, :-1]) & (srt[:, 1:] >= 0)
+            bt_entries += int(new.sum().item() + (srt[:, :1] >= 0).sum().item())
+    T, qn = prob.num_tokens, prob.num_heads_q
+    row_bytes = prob.kv_row_bytes()
+    idx_entries = T * (prob.ori_topk + prob.cmp_topk)
+    bytes_ = (attended * row_bytes + T * qn * prob.d_qk * 2 + T * qn * 512 * 2 + T * qn * 4 + idx_entries * 4
+              + bt_entries * 4 + prob.batch_size * 4 * 3)
+    flops = attended * qn * (2 * prob.d_qk + 2 * 512)
+    return {"attended_rows": attended, "bytes": bytes_, "flops": flops, "bt_entries": bt_entries}
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in sorted(glob.glob(os.path.join(ROOT, "sparse_shared_kv_gb300", "csrc", "*"))):
+        h.update(open(f, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def load_traffic(workload):
+    """DRAM bytes per launch of the dominant kernel from a committed ncu summary,
+    only while the kernel sources still hash to the captured version."""
+    path = os.path.join(ROOT, "profiles", f"traffic_{workload}.json")
+    try:
+        d = json.load(open(path))
+    except (OSError, ValueError):
+        return None
+    if d.get("source_hash") != kernel_source_hash():
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+def measured_peaks():
+    try:
+        d = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "of measured"
+    except (OSError, ValueError, KeyError):
+        return 6800.0, 1900.0, "of fallback"
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+def run_ours(args):
+    rank, world, local = dist_init("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import sparse_shared_kv_gb300 as sfm
+    sfm.build()
+    sfm.lib()
+
+    sets = [make_problem(args.workload, dev, 1000 + 97 * rank + i) for i in range(args.sets)]
+    acc = [accounting(p, sfm) for p in sets]
+    runners = []
+    for p in sets:
+        params = sfm.make_params(**p.attrs())
+        tens = sfm.make_tensors(p.t["q"], p.t["ori_kv"], **p.tensor_kwargs())
+        md = torch.empty(sfm.sfm_metadata_size(params), dtype=torch.int32, device=dev)
+        nb = sfm.sfm_workspace_size(params)
+        ws = torch.empty(nb, dtype=torch.uint8, device=dev) if nb else None
+        out = torch.empty(p.t["q"].shape[:-1] + (512,), dtype=p.torch_dtype, device=dev)
+        lse = torch.empty(p.num_tokens * p.num_heads_q, dtype=torch.float32, device=dev)
+        runners.append((p, params, tens, md, ws, out, lse))
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(k):
+        p, params, tens, md, ws, out, lse = runners[k % len(runners)]
+        sfm.sfm_metadata(params, tens, md, stream)
+        sfm.sfm_forward(params, tens, md, p.softmax_scale, out, lse, ws, status, stream)
+
+    gpu_uuid = str(torch.cuda.get_device_properties(dev).uuid)
+    sampler = ClockSampler(gpu_uuid if gpu_uuid.startswith("GPU-") else f"GPU-{gpu_uuid}")
+    sampler.start()
+    for k in range(max(args.warmup, 3)):
+        step(k)
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item()):#x} during warm-up")
+
+    K = args.steps
+    kb = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ke = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    t_in = sampler.mark()
+    e0.record(stream)
+    for k in range(K):
+        sfm.sfm_set_profile_events(kb[k], ke[k])
+        step(k)
+    sfm.sfm_set_profile_events(None, None)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    t_out = sampler.mark()
+    barrier(world)
+    ms_total = e0.elapsed_time(e1)
+    kernel_ms = [kb[k].elapsed_time(ke[k]) for k in range(K)]
+
+    # end to end through the public two-call API, inputs from pinned host memory
+    e2e = run_e2e(args, sfm, sets, acc, dev, stream)
+    sampler.stop()
+    clocks = sampler.summary(t_in, t_out)
+
+    ms_max = max_over_ranks(ms_total, world, dev)
+    rows_per_step = statistics.mean(a["attended_rows"] for a in acc)
+    rows_total = sum_over_ranks(sum(acc[k % len(acc)]["attended_rows"] for k in range(K)), world, dev)
+    flops_total = sum_over_ranks(sum(acc[k % len(acc)]["flops"] for k in range(K)), world, dev)
+    value = rows_total / (ms_max * 1e-3)
+    e2e_ms = max_over_ranks(e2e["ms_total"], world, dev)
+    e2e_rows = sum_over_ranks(e2e["rows"], world, dev)
+
+    hbm_peak, tc_peak, peak_note = measured_peaks()
+    bytes_launch = statistics.mean(acc[k % len(acc)]["bytes"] for k in range(K))
+    flops_launch = statistics.mean(acc[k % len(acc)]["flops"] for k in range(K))
+    kavg = statistics.mean(kernel_ms)
+    achieved_gbs = bytes_launch / (kavg * 1e-3) / 1e9
+    achieved_tf = flops_launch / (kavg * 1e-3) / 1e12
+    traffic = load_traffic(args.workload)
+    p0 = sets[0]
+
+    if rank == 0:
+        cpu = None
+        if world == 1 and not args.no_cpu_baseline:
+            cpu = cpu_baseline(args, sets[0], acc[0])
+        line = {
+            "metric": f"attended KV tokens/s ({args.workload.replace('_', ' ')}, 1 GB300 per rank)",
+            "value": value,
+            "unit": "tokens/s",
+            "n_gpus": world,
+            "steps": K,
+            "warmup": max(args.warmup, 3),
+            "ms_per_step": ms_max / K,
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "bf16",
+            "data": "synthetic (seeded generators, shapes and distributions of the pages' workloads)",
+            "config": {
+                "workload": args.workload, "batch": p0.batch_size, "q_n": p0.num_heads_q, "d": 512,
+                "d_qk": p0.d_qk, "cmp_topk": p0.cmp_topk, "ori_topk": p0.ori_topk, "cmp_ratio": p0.cmp_ratio,
+                "window": p0.ori_win_left + p0.ori_win_right + 1 if p0.ori_topk == 0 else 0,
+                "layout": f"{p0.layout_q}/{p0.layout_kv}", "attended_rows_per_step": rows_per_step,
+                "l2": f"inputs larger than L2: {args.sets} rotating input sets "
+                      f"({args.sets * bytes_launch / 1e6:.0f} MB of attended bytes)",
+                "step": "sfm_metadata (device planner) + sfm_forward (attention + combine)",
+                "parallelism": f"replicas x{world}",
+            },
+            "tflops": flops_total / (ms_max * 1e-3) / 1e12,
+            "roofline": {
+                "bound": "hbm", "achieved": achieved_gbs, "peak": hbm_peak, "unit": "GB/s",
+                "frac": achieved_gbs / hbm_peak, "traffic": traffic, "peak_note": peak_note,
+                "kernel": "sfm_attn (main attention kernel)", "kernel_ms_avg": kavg,
+                "algorithmic_bytes_per_launch": bytes_launch, "algorithmic_flops_per_launch": flops_launch,
+                "tensor_tflops": achieved_tf, "tensor_frac_of_bf16_peak": achieved_tf / tc_peak,
+            },
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_rows / (e2e_ms * 1e-3), "unit": "tokens/s",
+                    "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
+                    "ms_per_step": e2e_ms / e2e["steps"]},
+            "gpu_launches": 3 * K,
+            "clocks": clocks,
+        }
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_e2e(args, sfm, sets, acc, dev, stream):
+    """Public API, inputs H2D from pinned host memory, O / LSE D2H, per step."""
+    names = ("q", "cmp_sparse_indices", "ori_sparse_indices", "ori_block_table", "cmp_block_table",
+             "seqused_ori_kv", "seqused_cmp_kv", "cmp_residual_kv", "sinks")
+    host = []
+    for p in sets:
+        h = {n: p.t[n].cpu().pin_memory() for n in names if p.t[n] is not None}
+        out_h = torch.empty(p.t["q"].shape[:-1] + (512,), dtype=p.torch_dtype).pin_memory()
+        lse_h = torch.empty(p.num_tokens * p.num_heads_q, dtype=torch.float32).pin_memory()
+        host.append((h, out_h, lse_h))
+    h2d = sum(x.numel() * x.element_size() for x in host[0][0].values())
+    d2h = host[0][1].numel() * host[0][1].element_size() + host[0][2].numel() * 4
+
+    def step(k):
+        p = sets[k % len(sets)]
+        h, out_h, lse_h = host[k % len(sets)]
+        for n, x in h.items():
+            p.t[n].copy_(x, non_blocking=True)
+        T = p.t
+        md = sfm.sparse_flash_mla_metadata(
+            p.num_heads_q, 1, 512, cu_seqlens_q=T["cu_seqlens_q"], cu_seqlens_ori_kv=T["cu_seqlens_ori_kv"],
+            cu_seqlens_cmp_kv=T["cu_seqlens_cmp_kv"], seqused_ori_kv=T["seqused_ori_kv"],
+            seqused_cmp_kv=T["seqused_cmp_kv"], cmp_residual_kv=T["cmp_residual_kv"], batch_size=p.batch_size,
+            max_seqlen_q=p.max_seqlen_q, total_q=p.total_q, max_seqlen_ori_kv=p.max_seqlen_ori_kv,
+            max_seqlen_cmp_kv=p.max_seqlen_cmp_kv, ori_topk=p.ori_topk, cmp_topk=p.cmp_topk,
+            cmp_ratio=p.cmp_ratio, ori_mask_mode=p.ori_mask_mode, cmp_mask_mode=p.cmp_mask_mode,
+            ori_win_left=p.ori_win_left, ori_win_right=p.ori_win_right, layout_q=p.layout_q,
+            layout_kv=p.layout_kv, has_cmp_kv=p.has_cmp_kv, dtype=p.torch_dtype,
+            kv_format=1 if p.kv_format == "int8_packed" else 0, rope_head_dim=p.rope_head_dim,
+            ori_block_size=p.ori_block_size, cmp_block_size=p.cmp_block_size, return_softmax_lse=True,
+            device=dev, stream=stream)
+        out, lse = sfm.sparse_flash_mla(
+            T["q"], metadata=md, ori_kv=T["ori_kv"], cmp_kv=T["cmp_kv"], ori_sparse_indices=T["ori_sparse_indices"],
+            cmp_sparse_indices=T["cmp_sparse_indices"], ori_block_table=T["ori_block_table"],
+            cmp_block_table=T["cmp_block_table"], cu_seqlens_q=T["cu_seqlens_q"],
+            cu_seqlens_ori_kv=T["cu_seqlens_ori_kv"], cu_seqlens_cmp_kv=T["cu_seqlens_cmp_kv"],
+            seqused_ori_kv=T["seqused_ori_kv"], seqused_cmp_kv=T["seqused_cmp_kv"],
+            cmp_residual_kv=T["cmp_residual_kv"], sinks=T["sinks"], softmax_scale=p.softmax_scale,
+            ori_row_stride=p.ori_row_stride, cmp_row_stride=p.cmp_row_stride or None, stream=stream)
+        out_h.copy_(out, non_blocking=True)
+        lse_h.copy_(lse, non_blocking=True)
+
+    for k in range(3):
+        step(k)
+    torch.cuda.synchronize()
+    K = max(1, min(args.steps, 200))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for k in range(K):
+        step(k)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    rows = sum(acc[k % len(acc)]["attended_rows"] for k in range(K))
+    return {"ms_total": e0.elapsed_time(e1), "steps": K, "rows": rows, "h2d": h2d, "d2h": d2h}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle legs
+# ---------------------------------------------------------------------------
+def cpu_baseline(args, prob, acc, seconds=None):
+    import oracle
+    host = prob.to("cpu")
+    cores = os.cpu_count() or 1
+    seconds = args.cpu_seconds if seconds is None else seconds
+    t0 = time.time()
+    reps = 0
+    while True:
+        oracle.forward(host, nthreads=cores)
+        reps += 1
+        if time.time() - t0 >= seconds:
+            break
+    dt = time.time() - t0
+    return {"value": acc["attended_rows"] * reps / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"all {prob.num_tokens} query rows of one input set of the workload, {reps} pass(es), "
+                      f"{dt:.1f} s, fp64 C oracle with OpenMP"}
+
+
+def run_reference(args):
+    rank, world, local = dist_init("gloo")
+    if rank != 0:
+        return
+    import oracle
+    import sfm_inputs as S
+    oracle.build()
+    prob = S.WORKLOADS[args.workload](device="cpu", seed=1000)
+    cores = os.cpu_count() or 1
+    # attended rows per query row, from the oracle's own attended sets
+    b = oracle._Bound(prob)
+    counts = [len(oracle.attended(prob, t, b)[0]) for t in range(prob.num_tokens)]
+    per_step = 2                                   # query rows per step: keeps the run to minutes
+    W = max(args.warmup, 3)
+    K = args.steps
+
+    def step(k):
+        toks = [(k * per_step + j) % prob.num_tokens for j in range(per_step)]
+        oracle.forward(prob, toks, nthreads=cores)
+        return sum(counts[t] for t in toks)
+
+    for k in range(W):
+        step(k)
+    t0 = time.perf_counter()
+    rows = 0
+    for k in range(K):
+        rows += step(k)
+    dt = time.perf_counter() - t0
+    value = rows / dt
+    line = {
+        "impl": "reference",
+        "metric": f"attended KV tokens/s ({args.workload.replace('_', ' ')}, 1 GB300 per rank)",
+        "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": W,
+        "ms_per_step": dt * 1e3 / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic (seeded generators, shapes and distributions of the pages' workloads)",
+        "config": {"workload": args.workload, "batch": prob.batch_size, "q_n": prob.num_heads_q,
+                   "sample_per_step": f"{per_step} query rows of the batch"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{per_step} query rows per step (of {prob.num_tokens}), {K} steps"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+        return
+    run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

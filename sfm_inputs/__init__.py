@@ -101,6 +101,26 @@ class Problem:
         p.t = {k: (v.to(device) if isinstance(v, torch.Tensor) else v) for k, v in self.t.items()}
         return p
 
+    def attrs(self) -> dict:
+        """Scalar attributes under the names of the library's sfm_params."""
+        return dict(
+            num_heads_q=self.num_heads_q, num_heads_kv=1, head_dim=self.head_dim,
+            rope_head_dim=self.rope_head_dim, batch_size=self.batch_size, max_seqlen_q=self.max_seqlen_q,
+            total_q=self.total_q, max_seqlen_ori_kv=self.max_seqlen_ori_kv,
+            max_seqlen_cmp_kv=self.max_seqlen_cmp_kv, ori_topk=self.ori_topk, cmp_topk=self.cmp_topk,
+            cmp_ratio=self.cmp_ratio, ori_mask_mode=self.ori_mask_mode, cmp_mask_mode=self.cmp_mask_mode,
+            ori_win_left=self.ori_win_left, ori_win_right=self.ori_win_right, layout_q=self.layout_q,
+            layout_kv=self.layout_kv, has_ori_kv=1, has_cmp_kv=int(self.has_cmp_kv), dtype=self.dtype,
+            kv_format=1 if self.kv_format == "int8_packed" else 0, ori_block_size=self.ori_block_size,
+            cmp_block_size=self.cmp_block_size, return_lse=int(self.return_lse))
+
+    def tensor_kwargs(self) -> dict:
+        """Tensors (plus KV row strides) under the names of the library's sfm_tensors."""
+        d = {k: v for k, v in self.t.items() if k not in ("q", "ori_kv")}
+        d["ori_row_stride"] = self.ori_row_stride
+        d["cmp_row_stride"] = self.cmp_row_stride or None
+        return d
+
     def describe(self) -> str:
         return (f"{self.name}: q_n={self.num_heads_q} tokens={self.num_tokens} layout={self.layout_q}/"
                 f"{self.layout_kv} topk={self.ori_topk}/{self.cmp_topk} ratio={self.cmp_ratio} "

@@ -1,0 +1,264 @@
+// sfm_internal.cuh -- shared device/host definitions of the sfm library.
+//
+// Everything the planner, the attention kernels, the combine kernel and the
+// debug dump agree on lives here: the kernel parameter block, the metadata
+// layout, the per-query-row lengths and window, and the resolution of an
+// attended position to a KV row address.  The attended set follows the
+// "sparse_flash_mla" doc (zh), 参数说明 (ori_mask_mode, ori_win_left/right,
+// cmp_mask_mode, cmp_sparse_indices, cmp_residual_kv) and the right-down
+// alignment p = kv_len - q_len + i of its CP切分示例.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "sfm.h"
+
+namespace sfm {
+
+// ----------------------------------------------------------------------------
+// metadata layout (int32 words)
+//   [0, HDR)                      header (H_* below)
+//   [HDR, HDR+G+1)                worker split ranges: worker c owns splits [ws[c], ws[c+1])
+//   [.., +T+1)                    split prefix per query row: row t owns splits [sp[t], sp[t+1])
+//   [.., +T+1)                    cost prefix per query row (attended rows + per-split overhead)
+// ----------------------------------------------------------------------------
+constexpr int32_t kMetaMagic = 0x53464d31;   // "SFM1"
+constexpr int kHdr = 16;
+enum MetaHeader {
+    H_MAGIC = 0, H_FPRINT = 1, H_TOKENS = 2, H_WORKERS = 3, H_SPLIT = 4, H_PATH = 5,
+    H_TOTAL_SPLITS = 6, H_FLAGS = 7
+};
+// modelled cost of one split beyond its rows (Q load, partial write), in rows
+constexpr int kSplitOverheadRows = 32;
+
+__host__ __device__ inline int64_t meta_ws_off() { return kHdr; }
+__host__ __device__ inline int64_t meta_split_off(int G) { return kHdr + (int64_t)G + 1; }
+__host__ __device__ inline int64_t meta_cost_off(int G, int T) { return kHdr + (int64_t)G + 1 + (int64_t)T + 1; }
+__host__ __device__ inline int64_t meta_words(int G, int T)
+{
+    int64_t n = kHdr + (int64_t)G + 1 + 2 * ((int64_t)T + 1);
+    return n < 1024 ? 1024 : n;
+}
+
+enum PathId : int32_t { PATH_SIMT = 1, PATH_TC = 2 };
+
+// ----------------------------------------------------------------------------
+// kernel parameter block (passed by value)
+// ----------------------------------------------------------------------------
+struct KParams {
+    int32_t q_n, d_qk, d_v, rope;
+    int32_t batch, q_s, T;                 // T = query rows ("tokens")
+    int32_t ori_s, cmp_s;                  // BSND per-batch capacity
+    int32_t layout_q, layout_kv, dtype, packed;
+    int32_t ori_bs, cmp_bs, ori_bt_stride, cmp_bt_stride;
+    int64_t ori_row_stride, cmp_row_stride, ori_rows, cmp_rows;
+    int32_t ori_topk, cmp_topk, cmp_ratio, ori_mask_mode, cmp_mask_mode, win_left, win_right;
+    int32_t has_cmp, return_lse;
+    float scale;                            // softmax_scale
+    float scale_log2;                       // softmax_scale * log2(e)
+    // plan
+    int32_t G, split_rows, fingerprint, path;
+    int64_t ws_capacity_splits;
+    // tensors
+    const void *q;
+    const uint8_t *ori_kv, *cmp_kv;
+    const int32_t *ori_idx, *cmp_idx, *ori_bt, *cmp_bt;
+    const int32_t *cu_q, *cu_ori, *cu_cmp, *used_q, *used_ori, *used_cmp, *residual;
+    const float *sinks;
+    const int32_t *meta;
+    int32_t *meta_w;
+    void *out;
+    float *lse;
+    float *ws_o;      // [capacity][q_n][512] normalised partial O
+    float *ws_lse;    // [capacity][q_n] partial LSE
+    int32_t *status;
+    int32_t *dbg_rows;
+    int64_t dbg_cap;
+    int32_t *dbg_counts;
+};
+
+__device__ __forceinline__ void set_status(const KParams &kp, int bits)
+{
+    if (kp.status) atomicOr(kp.status, bits);
+}
+
+// ----------------------------------------------------------------------------
+// per query row: lengths, position, window, attended-position counts
+// ----------------------------------------------------------------------------
+struct Tok {
+    int32_t b, i, q_len, kv_len, cmp_len, p, p_cmp, valid;
+    int32_t lo, hi;        // ori window, inclusive (hi < lo: empty)
+    int32_t n_ori, n_cmp;  // attended positions of each source (topk entries or contiguous rows)
+};
+
+__device__ __forceinline__ int32_t clamp_len(const KParams &kp, int64_t v, int64_t cap)
+{
+    if (v < 0 || v > cap) {
+        set_status(kp, SFM_STATUS_BAD_LENGTH);
+        v = v < 0 ? 0 : cap;
+    }
+    return (int32_t)v;
+}
+
+__device__ inline Tok token_info(const KParams &kp, int t)
+{
+    Tok k;
+    int32_t qcap;
+    if (kp.layout_q == SFM_LAYOUT_BSND) {
+        k.b = t / kp.q_s;
+        k.i = t - k.b * kp.q_s;
+        qcap = kp.q_s;
+    } else {
+        int lo = 0, hi = kp.batch - 1;          // largest b with cu_q[b] <= t
+        while (lo < hi) {
+            int mid = (lo + hi + 1) >> 1;
+            if (__ldg(kp.cu_q + mid) <= t) lo = mid; else hi = mid - 1;
+        }
+        k.b = lo;
+        k.i = t - __ldg(kp.cu_q + lo);
+        qcap = __ldg(kp.cu_q + lo + 1) - __ldg(kp.cu_q + lo);
+    }
+    const int b = k.b;
+    k.q_len = kp.used_q ? clamp_len(kp, __ldg(kp.used_q + b), qcap) : qcap;
+
+    int64_t cap;
+    int64_t kv;
+    if (kp.layout_kv == SFM_LAYOUT_BSND) cap = kp.ori_s;
+    else if (kp.layout_kv == SFM_LAYOUT_TND) cap = __ldg(kp.cu_ori + b + 1) - __ldg(kp.cu_ori + b);
+    else cap = (int64_t)kp.ori_bt_stride * kp.ori_bs;
+    kv = kp.used_ori ? (int64_t)__ldg(kp.used_ori + b) : cap;
+    k.kv_len = clamp_len(kp, kv, cap);
+
+    k.cmp_len = 0;
+    if (kp.has_cmp) {
+        if (kp.layout_kv == SFM_LAYOUT_BSND) cap = kp.cmp_s;
+        else if (kp.layout_kv == SFM_LAYOUT_TND) cap = __ldg(kp.cu_cmp + b + 1) - __ldg(kp.cu_cmp + b);
+        else cap = (int64_t)kp.cmp_bt_stride * kp.cmp_bs;
+        int64_t c = kp.used_cmp ? (int64_t)__ldg(kp.used_cmp + b) : cap;
+        k.cmp_len = clamp_len(kp, c, cap);
+    }
+    const int64_t r = kp.residual ? (int64_t)__ldg(kp.residual + b) : 0;
+    k.p = k.kv_len - k.q_len + k.i;
+    const int64_t pc = (int64_t)k.cmp_len * kp.cmp_ratio + r - k.q_len + k.i;
+    k.p_cmp = (int32_t)pc;
+    k.valid = (t < kp.T) && (k.i < k.q_len);
+
+    // ori window [lo, hi]
+    int64_t lo = 0, hi = (int64_t)k.kv_len - 1, p = k.p;
+    if (kp.ori_mask_mode == 3) {
+        if (p < hi) hi = p;
+    } else if (kp.ori_mask_mode == 4) {
+        if (kp.win_left >= 0 && p - kp.win_left > lo) lo = p - kp.win_left;
+        if (kp.win_right >= 0 && p + kp.win_right < hi) hi = p + kp.win_right;
+    }
+    if (hi < lo) { lo = 0; hi = -1; }
+    k.lo = (int32_t)lo;
+    k.hi = (int32_t)hi;
+
+    k.n_ori = 0;
+    k.n_cmp = 0;
+    if (k.valid && k.kv_len > 0) k.n_ori = kp.ori_topk > 0 ? kp.ori_topk : (int32_t)(hi - lo + 1);
+    if (k.valid && kp.has_cmp && k.cmp_len > 0) {
+        if (kp.cmp_topk > 0) {
+            k.n_cmp = kp.cmp_topk;
+        } else if (kp.cmp_mask_mode == 3) {
+            int64_t v = (pc + 1) >= 0 ? (pc + 1) / kp.cmp_ratio : 0;   // slots j with (j+1)*ratio <= pc+1
+            k.n_cmp = (int32_t)(v < k.cmp_len ? v : k.cmp_len);
+        } else {
+            k.n_cmp = k.cmp_len;
+        }
+    }
+    return k;
+}
+
+// ----------------------------------------------------------------------------
+// attended position -> KV row
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ int64_t phys_row(const KParams &kp, int src, int b, int e)
+{
+    if (kp.layout_kv == SFM_LAYOUT_BSND) return (int64_t)b * (src ? kp.cmp_s : kp.ori_s) + e;
+    if (kp.layout_kv == SFM_LAYOUT_TND) return (int64_t)__ldg((src ? kp.cu_cmp : kp.cu_ori) + b) + e;
+    const int bs = src ? kp.cmp_bs : kp.ori_bs;
+    const int32_t *bt = src ? kp.cmp_bt : kp.ori_bt;
+    const int bts = src ? kp.cmp_bt_stride : kp.ori_bt_stride;
+    const int blk = __ldg(bt + (int64_t)b * bts + e / bs);
+    if (blk < 0) return -1;
+    return (int64_t)blk * bs + e % bs;
+}
+
+// Resolve attended position `pos` of query row t.  Returns the row address or
+// nullptr for a skipped entry; *logical receives the ori position or cmp slot
+// (-1 when skipped) and *src 0 (ori) / 1 (cmp).
+__device__ inline const uint8_t *resolve_row(const KParams &kp, const Tok &k, int t, int pos, int *logical,
+                                             int *src)
+{
+    int s, e;
+    bool ok;
+    if (pos < k.n_ori) {
+        s = 0;
+        if (kp.ori_topk > 0) {
+            e = __ldg(kp.ori_idx + (int64_t)t * kp.ori_topk + pos);
+            if (e >= k.kv_len) set_status(kp, SFM_STATUS_BAD_INDEX);
+            ok = e >= 0 && e < k.kv_len && e >= k.lo && e <= k.hi;
+        } else {
+            e = k.lo + pos;
+            ok = true;
+        }
+    } else {
+        s = 1;
+        const int j = pos - k.n_ori;
+        if (kp.cmp_topk > 0) {
+            e = __ldg(kp.cmp_idx + (int64_t)t * kp.cmp_topk + j);
+            if (e >= k.cmp_len) set_status(kp, SFM_STATUS_BAD_INDEX);
+            ok = e >= 0 && e < k.cmp_len &&
+                 (kp.cmp_mask_mode != 3 || (int64_t)(e + 1) * kp.cmp_ratio <= (int64_t)k.p_cmp + 1);
+        } else {
+            e = j;
+            ok = true;
+        }
+    }
+    *src = s;
+    if (!ok) {
+        *logical = -1;
+        return nullptr;
+    }
+    const int64_t row = phys_row(kp, s, k.b, e);
+    const int64_t nrows = s ? kp.cmp_rows : kp.ori_rows;
+    if (row < 0 || row >= nrows) {
+        set_status(kp, SFM_STATUS_BAD_BLOCK);
+        *logical = -1;
+        return nullptr;
+    }
+    *logical = e;
+    return (s ? kp.cmp_kv : kp.ori_kv) + row * (s ? kp.cmp_row_stride : kp.ori_row_stride);
+}
+
+// metadata sanity check shared by the kernels that consume a plan
+__device__ __forceinline__ bool meta_ok(const KParams &kp)
+{
+    const int32_t *m = kp.meta;
+    return m[H_MAGIC] == kMetaMagic && m[H_FPRINT] == kp.fingerprint && m[H_TOKENS] == kp.T &&
+           m[H_WORKERS] == kp.G && m[H_SPLIT] == kp.split_rows && m[H_PATH] == kp.path && m[H_FLAGS] == 0;
+}
+
+// first split of query row t / the row owning split w (binary search)
+__device__ __forceinline__ int split_owner(const int32_t *sp, int T, int w)
+{
+    int lo = 0, hi = T - 1;     // largest t with sp[t] <= w
+    while (lo < hi) {
+        int mid = (lo + hi + 1) >> 1;
+        if (sp[mid] <= w) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+// ----------------------------------------------------------------------------
+// host-side launchers (one per translation unit)
+// ----------------------------------------------------------------------------
+cudaError_t launch_plan(const KParams &kp, cudaStream_t st);
+cudaError_t launch_attn_simt(const KParams &kp, cudaStream_t st);
+cudaError_t launch_combine(const KParams &kp, cudaStream_t st);
+cudaError_t launch_debug(const KParams &kp, cudaStream_t st);
+
+}  // namespace sfm

@@ -1,0 +1,251 @@
+"""GPU parity: the CUDA library (through its C-ABI) against the CPU oracle.
+
+Tolerances (bf16 / fp16 inputs, fp32 accumulation, bf16 / fp16 output):
+|O_gpu - O_ref| <= 2e-2 + 2e-2 |O_ref| element-wise and |LSE_gpu - LSE_ref| <=
+1e-3; rows with an empty attended set must give exactly 0 and -inf.  Attended
+row sets are compared exactly through the library's debug dump.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import sfm_inputs as S
+import sparse_shared_kv_gb300 as sfm
+from tests import _sfm
+from tests.test_oracle_pins import _tiny_cases
+
+pytestmark = pytest.mark.gpu
+
+ATOL = 2e-2
+RTOL = 2e-2
+LSE_ATOL = 1e-3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    sfm.build()
+    torch.cuda.init()
+
+
+def assert_parity(prob, out, lse, tokens=None, host=None):
+    host = host or prob.to("cpu")
+    if tokens is None:
+        tokens = list(range(prob.num_tokens))
+    O_ref, L_ref = oracle.forward(host, tokens)
+    got = out.reshape(prob.num_tokens, prob.num_heads_q, 512)[tokens].float().cpu().numpy().astype(np.float64)
+    err = np.abs(got - O_ref)
+    bound = ATOL + RTOL * np.abs(O_ref)
+    bad = err > bound
+    assert not bad.any(), (f"{prob.name}: {bad.sum()} O elements out of tolerance, max err "
+                           f"{err.max():.3e} at {np.unravel_index(np.argmax(err - bound), err.shape)}")
+    if lse is not None:
+        gl = lse.reshape(prob.num_tokens, prob.num_heads_q)[tokens].cpu().numpy().astype(np.float64)
+        assert np.array_equal(np.isneginf(gl), np.isneginf(L_ref)), f"{prob.name}: -inf LSE pattern differs"
+        fin = np.isfinite(L_ref)
+        if fin.any():
+            d = np.abs(gl[fin] - L_ref[fin]).max()
+            assert d <= LSE_ATOL, f"{prob.name}: LSE max err {d:.3e}"
+        empty = np.isneginf(L_ref)
+        if empty.any():
+            assert np.all(got[empty] == 0.0)
+    return err.max()
+
+
+def assert_sets(prob, tokens=None, host=None):
+    host = host or prob.to("cpu")
+    sets, status = _sfm.debug_sets(prob)
+    assert status & ~sfm.STATUS_BAD_INDEX == 0, hex(status)
+    if tokens is None:
+        tokens = range(prob.num_tokens)
+    b = oracle._Bound(host)
+    for t in tokens:
+        src, pos = oracle.attended(host, t, b)
+        gs, gp = sets[t]
+        assert np.array_equal(gs, src) and np.array_equal(gp, pos), f"{prob.name}: token {t} attended set differs"
+
+
+# ---------------------------------------------------------------------------
+# tiny cases: every mode, layout, dtype, padded rows, packed rows, bad indices
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("name,kw", _tiny_cases(), ids=[c[0] for c in _tiny_cases()])
+def test_tiny_parity_and_sets(name, kw):
+    prob = S.build(name, seed=11, q_n=4, device="cuda", **kw)
+    if name == "csa_tnd_any_idx":
+        idx = prob.t["cmp_sparse_indices"]
+        idx[0, 0, 1] = idx[0, 0, 0]
+        idx[1, 0, 2] = 10_000
+        idx[2, 0, 0] = -7
+    out, lse, status = _sfm.run(prob)
+    expected = sfm.STATUS_BAD_INDEX if name == "csa_tnd_any_idx" else 0
+    assert status == expected, hex(status)
+    assert_parity(prob, out, lse)
+    assert_sets(prob)
+
+
+@pytest.mark.parametrize("q_n", [1, 2, 8, 16, 32, 48, 64, 128])
+def test_head_counts(q_n):
+    prob = S.build(f"heads{q_n}", seed=q_n, device="cuda", q_n=q_n, q_lens=[1, 1, 1], kv_lens=[700, 1500, 300],
+                   layout_q="BSND", layout_kv="PAGED", mode="csa", cmp_ratio=4, cmp_topk=96, sinks=True)
+    out, lse, status = _sfm.run(prob)
+    assert status == 0
+    assert_parity(prob, out, lse)
+
+
+# ---------------------------------------------------------------------------
+# the five workloads, reduced so the oracle checks every row
+# ---------------------------------------------------------------------------
+REDUCED = {
+    "swa_decode_tiny": lambda: S.swa_decode_tiny(device="cuda"),
+    "csa_decode_b4": lambda: S.csa_decode(device="cuda", batch=4),
+    "hca_decode_b2": lambda: S.hca_decode(device="cuda", batch=2),
+    "csa_prefill_small": lambda: S.csa_prefill(device="cuda", nseq=3, qmin=40, qmax=300, prefix_max=700),
+    "packed_decode_b3": lambda: S.packed_decode(device="cuda", batch=3, kv_len=8192),
+}
+
+
+@pytest.mark.parametrize("key", list(REDUCED))
+def test_reduced_workloads(key):
+    prob = REDUCED[key]()
+    out, lse, status = _sfm.run(prob)
+    assert status == 0, hex(status)
+    host = prob.to("cpu")
+    assert_parity(prob, out, lse, host=host)
+    assert_sets(prob, host=host)
+
+
+def test_fp16_and_lse_off():
+    prob = S.build("fp16_nolse", seed=5, device="cuda", q_n=64, q_lens=[1, 1], kv_lens=[900, 4000],
+                   layout_q="BSND", layout_kv="PAGED", mode="hca", cmp_ratio=16, dtype="fp16", sinks=True,
+                   return_lse=False)
+    out, lse, status = _sfm.run(prob)
+    assert lse is None and status == 0
+    assert_parity(prob, out, None)
+
+
+# ---------------------------------------------------------------------------
+# full sizes, sampled rows (the launch configuration the benchmark times)
+# ---------------------------------------------------------------------------
+def _sample(prob, n, extra=()):
+    g = torch.Generator().manual_seed(123)
+    T = prob.num_tokens
+    pick = set(torch.randperm(T, generator=g)[:n].tolist()) | {0, T - 1} | set(extra)
+    return sorted(t for t in pick if 0 <= t < T)
+
+
+@pytest.mark.parametrize("key", ["csa_decode", "hca_decode", "csa_prefill", "packed_decode"])
+def test_full_size_sampled(key):
+    prob = S.WORKLOADS[key](device="cuda")
+    out, lse, status = _sfm.run(prob)
+    assert status == 0, hex(status)
+    extra = ()
+    if key == "csa_prefill":
+        cu = prob.t["cu_seqlens_q"].tolist()
+        extra = [c + d for c in cu[:-1] for d in (0, 1, 129)] + [c - 1 for c in cu[1:]]
+    tokens = _sample(prob, 24 if key != "csa_prefill" else 64, extra)
+    host = prob.to("cpu")
+    assert_parity(prob, out, lse, tokens=tokens, host=host)
+    assert_sets(prob, tokens=tokens, host=host)
+    # properties that hold at any size: finite outputs, LSE finite where rows attend something
+    assert torch.isfinite(out.float()).all()
+
+
+# ---------------------------------------------------------------------------
+# properties of the library itself
+# ---------------------------------------------------------------------------
+def test_deterministic():
+    prob = S.csa_decode(device="cuda", batch=8)
+    r = _sfm.Runner(prob)
+    o1, l1, _ = r.run()
+    o1, l1 = o1.clone(), l1.clone()
+    o2, l2, _ = r.run()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_batch_invariance():
+    """A sequence's result is bitwise the same alone and inside a batch."""
+    prob = S.csa_decode(device="cuda", batch=6)
+    out, lse, _ = _sfm.run(prob)
+    out, lse = out.clone(), lse.clone()
+    for b in (0, 3, 5):
+        single = S.build("single", seed=0, device="cuda", q_n=64, q_lens=[1], kv_lens=[prob.kv_lens[b]],
+                         layout_q="BSND", layout_kv="PAGED", mode="csa", cmp_ratio=4, cmp_topk=512, sinks=True)
+        for k in ("ori_kv", "cmp_kv", "sinks"):
+            single.t[k] = prob.t[k]
+        single.t["q"] = prob.t["q"][b:b + 1].clone()
+        single.t["cmp_sparse_indices"] = prob.t["cmp_sparse_indices"][b:b + 1].clone()
+        single.t["ori_block_table"] = prob.t["ori_block_table"][b:b + 1].clone()
+        single.t["cmp_block_table"] = prob.t["cmp_block_table"][b:b + 1].clone()
+        for k in ("seqused_ori_kv", "seqused_cmp_kv", "cmp_residual_kv"):
+            single.t[k] = prob.t[k][b:b + 1].clone()
+        o1, l1, st = _sfm.run(single)
+        assert st == 0
+        assert torch.equal(o1[0], out[b]) and torch.equal(l1[0], lse[b]), b
+
+
+def test_context_parallel_split_on_gpu():
+    from tests.test_oracle_pins import _cp_slice
+    g = S.build("cp_global", seed=21, q_n=64, q_lens=[16, 18], kv_lens=[16, 18], cmp_lens=[4, 4],
+                residuals=[0, 2], layout_q="TND", layout_kv="TND", mode="csa", cmp_ratio=4, cmp_topk=512,
+                index_mode="all_visible", sinks=True)
+    r0 = _cp_slice(g, [(0, 16), (16, 24)], [(0, 16), (16, 24)], [(0, 4), (4, 6)], [16, 8], [16, 8], [4, 2], [0, 0])
+    r1 = _cp_slice(g, [(24, 34)], [(16, 34)], [(4, 8)], [10], [18], [4], [2])
+    outs = []
+    for p in (g, r0, r1):
+        pg = p.to("cuda")
+        o, l, st = _sfm.run(pg)
+        assert st == 0
+        assert_parity(pg, o, l, host=p)
+        outs.append(o.cpu())
+    assert torch.equal(torch.cat([outs[1], outs[2]]), outs[0])
+
+
+def test_bad_values_are_flagged_not_faulted():
+    prob = S.build("bad", seed=3, device="cuda", q_n=8, q_lens=[1, 1], kv_lens=[300, 500], layout_q="BSND",
+                   layout_kv="PAGED", mode="csa", cmp_ratio=4, cmp_topk=16, sinks=True)
+    prob.t["cmp_sparse_indices"][0, 0, 0, 3] = 1 << 20            # beyond cmp_len
+    prob.t["ori_block_table"][1, 2] = 1 << 24                     # beyond the cache
+    out, lse, status = _sfm.run(prob)
+    assert status & sfm.STATUS_BAD_INDEX and status & sfm.STATUS_BAD_BLOCK
+    assert torch.isfinite(out.float()).all()
+    # the rows that stayed valid still match the oracle (which skips the same entries)
+    host = prob.to("cpu")
+    host.t["ori_block_table"][1, 2] = 0
+    O_ref, _ = oracle.forward(host, [0])
+    got = out[0].float().cpu().numpy()
+    assert np.all(np.abs(got - O_ref[0]) <= ATOL + RTOL * np.abs(O_ref[0]))
+
+
+def test_metadata_mismatch_zeroes_outputs():
+    prob = S.csa_decode(device="cuda", batch=2)
+    r = _sfm.Runner(prob)
+    r.run()
+    other = _sfm.params_of(prob, ori_win_left=63)
+    md = torch.empty(sfm.sfm_metadata_size(other), dtype=torch.int32, device="cuda")
+    sfm.sfm_metadata(other, r.tensors, md)
+    r.status.zero_()
+    sfm.sfm_forward(r.params, r.tensors, md, prob.softmax_scale, r.out, r.lse, r.ws, r.status)
+    torch.cuda.synchronize()
+    assert int(r.status.item()) & sfm.STATUS_METADATA_MISMATCH
+    assert torch.count_nonzero(r.out.float()) == 0 and torch.isneginf(r.lse).all()
+
+
+def test_public_two_call_api():
+    prob = S.csa_decode(device="cuda", batch=3)
+    T = prob.t
+    md = sfm.sparse_flash_mla_metadata(
+        64, 1, 512, seqused_ori_kv=T["seqused_ori_kv"], seqused_cmp_kv=T["seqused_cmp_kv"],
+        cmp_residual_kv=T["cmp_residual_kv"], batch_size=3, max_seqlen_q=1, max_seqlen_ori_kv=prob.max_seqlen_ori_kv,
+        max_seqlen_cmp_kv=prob.max_seqlen_cmp_kv, cmp_topk=512, cmp_ratio=4, ori_mask_mode=4, cmp_mask_mode=3,
+        ori_win_left=127, ori_win_right=0, layout_q="BSND", layout_kv="PAGED", ori_block_size=128,
+        cmp_block_size=128, return_softmax_lse=True)
+    out, lse = sfm.sparse_flash_mla(
+        T["q"], metadata=md, ori_kv=T["ori_kv"], cmp_kv=T["cmp_kv"], cmp_sparse_indices=T["cmp_sparse_indices"],
+        ori_block_table=T["ori_block_table"], cmp_block_table=T["cmp_block_table"],
+        seqused_ori_kv=T["seqused_ori_kv"], seqused_cmp_kv=T["seqused_cmp_kv"],
+        cmp_residual_kv=T["cmp_residual_kv"], sinks=T["sinks"], softmax_scale=1 / math.sqrt(512))
+    torch.cuda.synchronize()
+    assert out.shape == T["q"].shape
+    assert_parity(prob, out, lse)
