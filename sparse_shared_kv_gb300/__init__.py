@@ -129,6 +129,9 @@ def _stream(stream) -> Optional[int]:
 def sfm_set_profile_events(begin=None, end=None) -> None:
     """Record ``begin`` / ``end`` (torch.cuda.Event) around the main attention
     kernel of the following sfm_forward calls; ``None, None`` turns it off."""
+    for ev in (begin, end):
+        if ev is not None and ev.cuda_event == 0:
+            ev.record()          # torch creates the underlying cudaEvent_t lazily
     b = begin.cuda_event if begin is not None else None
     e = end.cuda_event if end is not None else None
     _check("sfm_set_profile_events", lib().sfm_set_profile_events(b, e))

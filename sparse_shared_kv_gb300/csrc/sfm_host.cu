@@ -180,6 +180,8 @@ void fill_common(KParams &kp, const sfm_params &p, const Plan &pl)
     kp.T = (int32_t)pl.T;
     kp.ori_s = p.layout_kv == SFM_LAYOUT_BSND ? p.max_seqlen_ori_kv : 0;
     kp.cmp_s = p.layout_kv == SFM_LAYOUT_BSND ? p.max_seqlen_cmp_kv : 0;
+    kp.ori_max = p.max_seqlen_ori_kv;
+    kp.cmp_max = p.max_seqlen_cmp_kv;
     kp.layout_q = p.layout_q;
     kp.layout_kv = p.layout_kv;
     kp.dtype = p.dtype;

@@ -50,6 +50,7 @@ struct KParams {
     int32_t q_n, d_qk, d_v, rope;
     int32_t batch, q_s, T;                 // T = query rows ("tokens")
     int32_t ori_s, cmp_s;                  // BSND per-batch capacity
+    int32_t ori_max, cmp_max;              // paged: declared max lengths (length capacity)
     int32_t layout_q, layout_kv, dtype, packed;
     int32_t ori_bs, cmp_bs, ori_bt_stride, cmp_bt_stride;
     int64_t ori_row_stride, cmp_row_stride, ori_rows, cmp_rows;
@@ -126,7 +127,7 @@ __device__ inline Tok token_info(const KParams &kp, int t)
     int64_t kv;
     if (kp.layout_kv == SFM_LAYOUT_BSND) cap = kp.ori_s;
     else if (kp.layout_kv == SFM_LAYOUT_TND) cap = __ldg(kp.cu_ori + b + 1) - __ldg(kp.cu_ori + b);
-    else cap = (int64_t)kp.ori_bt_stride * kp.ori_bs;
+    else cap = kp.ori_max;      // paged: the declared max length (the planner sees no block table)
     kv = kp.used_ori ? (int64_t)__ldg(kp.used_ori + b) : cap;
     k.kv_len = clamp_len(kp, kv, cap);
 
@@ -134,7 +135,7 @@ __device__ inline Tok token_info(const KParams &kp, int t)
     if (kp.has_cmp) {
         if (kp.layout_kv == SFM_LAYOUT_BSND) cap = kp.cmp_s;
         else if (kp.layout_kv == SFM_LAYOUT_TND) cap = __ldg(kp.cu_cmp + b + 1) - __ldg(kp.cu_cmp + b);
-        else cap = (int64_t)kp.cmp_bt_stride * kp.cmp_bs;
+        else cap = kp.cmp_max;
         int64_t c = kp.used_cmp ? (int64_t)__ldg(kp.used_cmp + b) : cap;
         k.cmp_len = clamp_len(kp, c, cap);
     }
@@ -182,6 +183,7 @@ __device__ __forceinline__ int64_t phys_row(const KParams &kp, int src, int b, i
     const int bs = src ? kp.cmp_bs : kp.ori_bs;
     const int32_t *bt = src ? kp.cmp_bt : kp.ori_bt;
     const int bts = src ? kp.cmp_bt_stride : kp.ori_bt_stride;
+    if (e / bs >= bts) return -1;     // beyond the block table row
     const int blk = __ldg(bt + (int64_t)b * bts + e / bs);
     if (blk < 0) return -1;
     return (int64_t)blk * bs + e % bs;

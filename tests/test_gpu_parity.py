@@ -199,7 +199,11 @@ def test_context_parallel_split_on_gpu():
         assert st == 0
         assert_parity(pg, o, l, host=p)
         outs.append(o.cpu())
-    assert torch.equal(torch.cat([outs[1], outs[2]]), outs[0])
+    # the global call is prefill-shaped (one split per row) and the rank calls are
+    # decode-shaped (fixed-size splits merged by the combine), so the two agree
+    # to rounding, not bit for bit
+    d = (torch.cat([outs[1], outs[2]]).float() - outs[0].float()).abs()
+    assert d.max().item() <= ATOL
 
 
 def test_bad_values_are_flagged_not_faulted():
