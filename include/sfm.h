@@ -102,6 +102,7 @@ enum sfm_error {
 #define SFM_STATUS_METADATA_MISMATCH  0x08  /* metadata built for other params: outputs zeroed */
 #define SFM_STATUS_WORKSPACE_OVERFLOW 0x10  /* plan needs more workspace than given: outputs zeroed */
 #define SFM_STATUS_PLAN_OVERFLOW      0x20  /* plan larger than int32 counters allow: outputs zeroed */
+#define SFM_STATUS_TIMEOUT            0x40  /* a kernel pipeline wait gave up (bounded spin): outputs undefined */
 
 /* Scalar attributes shared by sfm_metadata() and sfm_forward().  Field names
  * follow the pages' parameter tables ("sparse_flash_mla" doc, 参数说明). */
@@ -131,6 +132,8 @@ typedef struct sfm_params {
     int32_t ori_block_size;    /* paged: rows per ori block, multiple of 16, <= 1024 */
     int32_t cmp_block_size;    /* paged with cmp_kv: rows per cmp block, multiple of 16, <= 1024 */
     int32_t return_lse;        /* 1: write LSE (fp32, token-major x q_n) */
+    int32_t kernel_hint;       /* 0: automatic; 1: CUDA-core kernel; 2: tensor-core kernel
+                                  (SFM_ERR_UNSUPPORTED when the params do not fit it) */
 } sfm_params;
 
 /* Device tensors of one call.  Shapes (row = one KV row of row_stride bytes):

@@ -46,7 +46,7 @@ class SfmParams(C.Structure):
         "num_heads_q", "num_heads_kv", "head_dim", "rope_head_dim", "batch_size", "max_seqlen_q", "total_q",
         "max_seqlen_ori_kv", "max_seqlen_cmp_kv", "ori_topk", "cmp_topk", "cmp_ratio", "ori_mask_mode",
         "cmp_mask_mode", "ori_win_left", "ori_win_right", "layout_q", "layout_kv", "has_ori_kv", "has_cmp_kv",
-        "dtype", "kv_format", "ori_block_size", "cmp_block_size", "return_lse")]
+        "dtype", "kv_format", "ori_block_size", "cmp_block_size", "return_lse", "kernel_hint")]
 
     def as_dict(self):
         return {n: getattr(self, n) for n, _ in self._fields_}
@@ -237,7 +237,7 @@ def make_params(**kw) -> SfmParams:
     defaults = dict(num_heads_kv=1, head_dim=512, rope_head_dim=0, total_q=0, max_seqlen_cmp_kv=0, ori_topk=0,
                     cmp_topk=0, cmp_ratio=1, ori_mask_mode=4, cmp_mask_mode=3, ori_win_left=-1, ori_win_right=-1,
                     layout_q=BSND, layout_kv=BSND, has_ori_kv=1, has_cmp_kv=0, dtype=BF16, kv_format=KV_PLAIN,
-                    ori_block_size=0, cmp_block_size=0, return_lse=0)
+                    ori_block_size=0, cmp_block_size=0, return_lse=0, kernel_hint=0)
     defaults.update(kw)
     for k, v in defaults.items():
         if k in ("layout_q", "layout_kv") and isinstance(v, str):

@@ -67,7 +67,14 @@ int validate_params(const sfm_params *pp)
             return SFM_ERR_LAYOUT;
     }
     if (p.return_lse != 0 && p.return_lse != 1) return SFM_ERR_INVALID_ARG;
+    if (p.kernel_hint < 0 || p.kernel_hint > 2) return SFM_ERR_INVALID_ARG;
     return SFM_OK;
+}
+
+// The tensor-core kernel covers plain bf16 / fp16 rows with up to 64 heads.
+bool tc_fits(const sfm_params &p)
+{
+    return p.kv_format == SFM_KV_PLAIN && p.num_heads_q <= 64;
 }
 
 // Required length tensors (both calls): 参数组约束 / Paged Attention参数组.
@@ -127,11 +134,13 @@ int make_plan(const sfm_params &p, Plan *pl)
     int sms = 0;
     int rc = num_sms(&sms);
     if (rc) return rc;
-    pl->path = PATH_SIMT;
+    if (p.kernel_hint == 2 && !tc_fits(p)) return SFM_ERR_UNSUPPORTED;
+    pl->path = (p.kernel_hint == 1 || !tc_fits(p)) ? PATH_SIMT : PATH_TC;
     pl->G = sms;
     pl->T = num_tokens(p);
     const bool decode_like = p.max_seqlen_q <= 16;
-    pl->split_rows = decode_like ? 256 : (1 << 30);
+    // tensor-core tiles are 64 rows: splits of 3 tiles
+    pl->split_rows = decode_like ? (pl->path == PATH_TC ? 192 : 256) : (1 << 30);
     const int64_t mp = max_positions(p);
     pl->max_splits_per_token = decode_like ? (mp + pl->split_rows - 1) / pl->split_rows : 1;
     return SFM_OK;
@@ -368,7 +377,8 @@ int sfm_forward(const sfm_params *params, const sfm_tensors *in, const int32_t *
     }
     cudaStream_t st = (cudaStream_t)stream;
     if (g_prof_begin && cudaEventRecord(g_prof_begin, st) != cudaSuccess) return SFM_ERR_CUDA;
-    if (launch_attn_simt(kp, st) != cudaSuccess) return SFM_ERR_CUDA;
+    const cudaError_t le = pl.path == PATH_TC ? launch_attn_tc(kp, st) : launch_attn_simt(kp, st);
+    if (le != cudaSuccess) return SFM_ERR_CUDA;
     if (g_prof_end && cudaEventRecord(g_prof_end, st) != cudaSuccess) return SFM_ERR_CUDA;
     if (launch_combine(kp, st) != cudaSuccess) return SFM_ERR_CUDA;
     return SFM_OK;

@@ -260,6 +260,7 @@ __device__ __forceinline__ int split_owner(const int32_t *sp, int T, int w)
 // ----------------------------------------------------------------------------
 cudaError_t launch_plan(const KParams &kp, cudaStream_t st);
 cudaError_t launch_attn_simt(const KParams &kp, cudaStream_t st);
+cudaError_t launch_attn_tc(const KParams &kp, cudaStream_t st);
 cudaError_t launch_combine(const KParams &kp, cudaStream_t st);
 cudaError_t launch_debug(const KParams &kp, cudaStream_t st);
 

@@ -80,9 +80,15 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     return true;
 }
 
-__device__ __forceinline__ void named_bar_sync(int id, int nthreads)
+// Warp-uniform bounded wait: lane 0 polls, the warp then reconverges and
+// every lane gets the same verdict, so control flow never diverges inside a
+// warp on a timeout (warp collectives after the wait stay safe).
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int *abort)
 {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+    bool ok = true;
+    if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort);
+    __syncwarp();
+    return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
 }
 
 // ---------------------------------------------------------------------------

@@ -253,3 +253,47 @@ def test_public_two_call_api():
     torch.cuda.synchronize()
     assert out.shape == T["q"].shape
     assert_parity(prob, out, lse)
+
+
+# ---------------------------------------------------------------------------
+# both attention kernels on the shapes the tensor-core kernel covers
+# ---------------------------------------------------------------------------
+def _plain_cases():
+    return [c for c in _tiny_cases() if "packed" not in c[0]]
+
+
+@pytest.mark.parametrize("hint", [1, 2], ids=["cuda_core", "tensor_core"])
+@pytest.mark.parametrize("name,kw", _plain_cases(), ids=[c[0] for c in _plain_cases()])
+def test_kernel_paths_tiny(name, kw, hint):
+    prob = S.build(name, seed=17, q_n=4, device="cuda", **kw)
+    out, lse, status = _sfm.Runner(prob, params=_sfm.params_of(prob, kernel_hint=hint)).run()
+    assert status == 0, hex(status)
+    assert_parity(prob, out, lse)
+
+
+@pytest.mark.parametrize("hint", [1, 2], ids=["cuda_core", "tensor_core"])
+@pytest.mark.parametrize("q_n", [1, 8, 16, 32, 40, 64])
+def test_kernel_paths_heads(q_n, hint):
+    prob = S.build(f"heads{q_n}", seed=100 + q_n, device="cuda", q_n=q_n, q_lens=[1, 1, 1, 1],
+                   kv_lens=[700, 1500, 300, 20000], layout_q="BSND", layout_kv="PAGED", mode="csa", cmp_ratio=4,
+                   cmp_topk=384, sinks=True)
+    out, lse, status = _sfm.Runner(prob, params=_sfm.params_of(prob, kernel_hint=hint)).run()
+    assert status == 0, hex(status)
+    assert_parity(prob, out, lse)
+
+
+@pytest.mark.parametrize("hint", [1, 2], ids=["cuda_core", "tensor_core"])
+def test_kernel_paths_prefill_fp16(hint):
+    prob = S.build("prefill_fp16", seed=23, device="cuda", q_n=64, q_lens=[70, 130], kv_lens=[200, 900],
+                   layout_q="TND", layout_kv="PAGED", mode="hca", cmp_ratio=4, dtype="fp16", sinks=True,
+                   ori_block_size=64, cmp_block_size=32)
+    out, lse, status = _sfm.Runner(prob, params=_sfm.params_of(prob, kernel_hint=hint)).run()
+    assert status == 0, hex(status)
+    assert_parity(prob, out, lse)
+
+
+def test_tensor_core_hint_rejects_unsupported():
+    prob = S.build("q128", seed=1, device="cuda", q_n=128, q_lens=[1], kv_lens=[300], layout_q="BSND",
+                   layout_kv="BSND", mode="swa")
+    with pytest.raises(sfm.SfmError):
+        sfm.sfm_metadata_size(_sfm.params_of(prob, kernel_hint=2))
