@@ -70,14 +70,30 @@ struct SplitInfo {
     Tok k;
 };
 
+// The split's row and that row's lengths / window / position counts come
+// from the plan (two dependent loads instead of a search and a length walk).
 __device__ __forceinline__ SplitInfo split_info(const KParams &kp, const int32_t *sp, int w)
 {
     SplitInfo s;
-    s.t = split_owner(sp, kp.T, w);
-    s.nsplit = sp[s.t + 1] - sp[s.t];
-    s.sidx = w - sp[s.t];
-    s.k = token_info(kp, s.t);
-    const int n = s.k.n_ori + s.k.n_cmp;
+    s.t = kp.meta[meta_own_off(kp.G, kp.T) + w];
+    const int32_t *rec = kp.meta + meta_rec_off(kp.G, kp.T) + (int64_t)kRecWords * s.t;
+    const int s_beg = sp[s.t], s_end = sp[s.t + 1];
+    s.nsplit = s_end - s_beg;
+    s.sidx = w - s_beg;
+    Tok &k = s.k;
+    k.b = rec[0];
+    k.kv_len = rec[1];
+    k.cmp_len = rec[2];
+    k.p_cmp = rec[3];
+    k.lo = rec[4];
+    k.hi = rec[5];
+    k.n_ori = rec[6];
+    k.n_cmp = rec[7];
+    k.i = 0;
+    k.q_len = 0;
+    k.p = 0;
+    k.valid = 1;
+    const int n = k.n_ori + k.n_cmp;
     s.pos0 = s.sidx * kp.split_rows;
     s.pos1 = min(n, s.pos0 + kp.split_rows);
     const int rows = s.pos1 > s.pos0 ? s.pos1 - s.pos0 : 0;
@@ -184,12 +200,22 @@ __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(KParams kp)
                 cp_async_commit();
                 pend_bar[pend++] = bar(B_Q_FULL);
             }
+            // rows of tile 0 resolve while Q streams in; tile i+1 resolves while
+            // tile i streams in and while waiting for a free stage
+            auto resolve = [&](int i) -> const uint8_t * {
+                const int pos = s.pos0 + i * NT + pt;
+                if (pos >= s.pos1) return nullptr;
+                int logical, src;
+                return resolve_row(kp, s.k, s.t, pos, &logical, &src);
+            };
+            const uint8_t *rp = resolve(0);
+            const uint8_t *rp_next = s.ntiles > 1 ? resolve(1) : nullptr;   // independent chains overlap
             for (int i = 0; i < s.ntiles; ++i, ++g) {
                 const int st = g & 1, use = g >> 1;
                 if (use >= 1) {
                     // never block while holding copies whose arrival is deferred:
                     // the MMA warp may be waiting for exactly those rows
-                    const bool ready = __all_sync(0xffffffffu, mbar_try_wait(bar(B_KV_EMPTY + st), (use - 1) & 1));
+                    const bool ready = __all_sync(0xffffffffu, mbar_test(bar(B_KV_EMPTY + st), (use - 1) & 1));
                     if (!ready) {
                         while (pend) flush_one();
                         if (!warp_wait(bar(B_KV_EMPTY + st), (use - 1) & 1, abort_flag)) {
@@ -197,12 +223,6 @@ __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(KParams kp)
                             break;
                         }
                     }
-                }
-                const int pos = s.pos0 + i * NT + pt;
-                const uint8_t *rp = nullptr;
-                if (pos < s.pos1) {
-                    int logical, src;
-                    rp = resolve_row(kp, s.k, s.t, pos, &logical, &src);
                 }
                 __syncwarp();
                 const uint32_t vm = __ballot_sync(0xffffffffu, rp != nullptr);
@@ -214,6 +234,8 @@ __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(KParams kp)
                 }
                 cp_async_commit();
                 pend_bar[pend++] = bar(B_KV_FULL + st);
+                rp = rp_next;
+                rp_next = i + 2 < s.ntiles ? resolve(i + 2) : nullptr;
                 while (pend > 1) flush_one();
             }
             ++ks;
@@ -222,6 +244,9 @@ __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(KParams kp)
         cp_async_wait<0>();
     } else if (warp == 2) {
         // ======================= MMA issuer =======================
+        // One thread polls both inputs and issues whichever product is ready:
+        // S(i) needs tile i staged and its S buffer free; P.V(i) needs P(i)
+        // (and, for a split's first tile, the previous epilogue done with O).
         if (lane == 0) {
             const uint32_t id_s = idesc_f16(128, 64, bf16, false, false);
             const uint32_t id_pv = idesc_f16(128, 256, bf16, false, true);
@@ -231,45 +256,60 @@ __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(KParams kp)
                 const SplitInfo s = split_info(kp, sp, w);
                 if (!mbar_wait(bar(B_Q_FULL), ks & 1, abort_flag)) break;
                 tc_fence_after();
-                for (int i = 0; i <= s.ntiles && !stop; ++i) {
-                    if (i < s.ntiles) {
-                        const int gi = g + i, st = gi & 1;
-                        if (!mbar_wait(bar(B_KV_FULL + st), (gi >> 1) & 1, abort_flag)) { stop = true; break; }
-                        if (gi >= 2 && !mbar_wait(bar(B_S_FREE + st), ((gi >> 1) - 1) & 1, abort_flag)) {
-                            stop = true;
-                            break;
+                int ns = 0, npv = 0;             // next tile to issue S / P.V for
+                uint64_t t_idle = 0;
+                while (npv < s.ntiles) {
+                    bool progressed = false;
+                    if (ns < s.ntiles) {
+                        const int gi = g + ns, st = gi & 1;
+                        if (mbar_test(bar(B_KV_FULL + st), (gi >> 1) & 1) &&
+                            (gi < 2 || mbar_test(bar(B_S_FREE + st), ((gi >> 1) - 1) & 1))) {
+                            tc_fence_after();
+                            const uint32_t d = tmem + TM_S + st * 64;
+                            const uint32_t kv = sb + KV_OFF + st * KV_STAGE;
+#pragma unroll 8
+                            for (int k = 0; k < 32; ++k) {
+                                const uint32_t off = (k >> 2) * 8192u + (k & 3) * 32u;
+                                umma_f16(d, sdesc_sw128(sb + Q_OFF + off, 16, 1024),
+                                         sdesc_sw128(kv + off, 16, 1024), id_s, k > 0);
+                            }
+                            umma_commit(bar(B_S_FULL + st));
+                            if (ns == s.ntiles - 1) umma_commit(bar(B_Q_EMPTY));
+                            ++ns;
+                            progressed = true;
                         }
-                        tc_fence_after();
-                        const uint32_t d = tmem + TM_S + st * 64;
-                        const uint32_t kv = sb + KV_OFF + st * KV_STAGE;
-#pragma unroll 4
-                        for (int k = 0; k < 32; ++k) {
-                            const uint32_t off = (k >> 2) * 8192u + (k & 3) * 32u;
-                            umma_f16(d, sdesc_sw128(sb + Q_OFF + off, 16, 1024), sdesc_sw128(kv + off, 16, 1024),
-                                     id_s, k > 0);
-                        }
-                        umma_commit(bar(B_S_FULL + st));
-                        if (i == s.ntiles - 1) umma_commit(bar(B_Q_EMPTY));
                     }
-                    if (i >= 1) {
-                        const int gj = g + i - 1, st = gj & 1;
-                        if (!mbar_wait(bar(B_P_FULL), gj & 1, abort_flag)) { stop = true; break; }
-                        if (i == 1 && ks >= 1 && !mbar_wait(bar(B_O_FREE), (ks - 1) & 1, abort_flag)) {
+                    if (npv < ns) {
+                        const int gj = g + npv, st = gj & 1;
+                        if (mbar_test(bar(B_P_FULL), gj & 1) &&
+                            (npv > 0 || ks == 0 || mbar_test(bar(B_O_FREE), (ks - 1) & 1))) {
+                            tc_fence_after();
+                            const uint32_t kv = sb + KV_OFF + st * KV_STAGE;
+#pragma unroll
+                            for (int k = 0; k < 8; ++k) {
+                                const int half = k >> 2, sub = k & 3;
+                                const uint32_t a = sb + P_OFF + (half ? 0u : 8192u) + sub * 32u;
+                                const uint32_t b = kv + half * 32768u + sub * 2048u;
+                                umma_f16(tmem + TM_O, sdesc_sw128(a, 16, 1024), sdesc_sw128(b, 8192, 1024), id_pv,
+                                         !(npv == 0 && k == 0));
+                            }
+                            umma_commit(bar(B_KV_EMPTY + st));
+                            umma_commit(bar(B_O_DONE));
+                            ++npv;
+                            progressed = true;
+                        }
+                    }
+                    if (progressed) {
+                        t_idle = 0;
+                    } else {
+                        if (*abort_flag) { stop = true; break; }
+                        const uint64_t now = globaltimer_ns();
+                        if (t_idle == 0) t_idle = now;
+                        else if (now - t_idle > kTimeoutNs) {
+                            *abort_flag = 1;
                             stop = true;
                             break;
                         }
-                        tc_fence_after();
-                        const uint32_t kv = sb + KV_OFF + st * KV_STAGE;
-#pragma unroll
-                        for (int k = 0; k < 8; ++k) {
-                            const int half = k >> 2, sub = k & 3;
-                            const uint32_t a = sb + P_OFF + (half ? 0u : 8192u) + sub * 32u;
-                            const uint32_t b = kv + half * 32768u + sub * 2048u;
-                            umma_f16(tmem + TM_O, sdesc_sw128(a, 16, 1024), sdesc_sw128(b, 8192, 1024), id_pv,
-                                     !(i == 1 && k == 0));
-                        }
-                        umma_commit(bar(B_KV_EMPTY + st));
-                        umma_commit(bar(B_O_DONE));
                     }
                 }
                 g += s.ntiles;

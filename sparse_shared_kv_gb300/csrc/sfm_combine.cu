@@ -23,22 +23,30 @@ namespace sfm {
 
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kMaxSplits = 64;    // per row, merged from shared memory in chunks of this size
+constexpr int kThreads = 256;                 // 8 warps, one head each
+constexpr int kHeadsPerBlock = kThreads / 32;
 
-__device__ __forceinline__ uint16_t to_half(float f, int dtype)
+__device__ __forceinline__ uint32_t to_half2(float a, float b, int dtype)
 {
-    if (dtype == SFM_DTYPE_BF16) return __bfloat16_as_ushort(__float2bfloat16_rn(f));
-    return __half_as_ushort(__float2half_rn(f));
+    if (dtype == SFM_DTYPE_BF16) {
+        __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+        return *reinterpret_cast<uint32_t *>(&v);
+    }
+    __half2 v = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t *>(&v);
 }
 
+// grid (query rows, ceil(q_n / 8)); warp = head, lane = 16 consecutive dims
 __global__ void __launch_bounds__(kThreads) sfm_combine_kernel(KParams kp)
 {
-    __shared__ float s_w[kMaxSplits];
-    __shared__ float s_red[2];
-    const int t = blockIdx.x, tid = threadIdx.x;
+    const int t = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int h = blockIdx.y * kHeadsPerBlock + warp;
     const bool ok = meta_ok(kp);
-    if (!ok && t == 0 && tid == 0) set_status(kp, SFM_STATUS_METADATA_MISMATCH | kp.meta[H_FLAGS]);
+    if (t == 0 && blockIdx.y == 0 && threadIdx.x == 0) {
+        if (!ok) set_status(kp, SFM_STATUS_METADATA_MISMATCH | kp.meta[H_FLAGS]);
+        else if (kp.meta[H_LENFLAGS]) set_status(kp, kp.meta[H_LENFLAGS]);
+    }
+    if (h >= kp.q_n) return;
     int ns = 0, s0 = 0;
     if (ok) {
         const int32_t *sp = kp.meta + meta_split_off(kp.G);
@@ -46,55 +54,55 @@ __global__ void __launch_bounds__(kThreads) sfm_combine_kernel(KParams kp)
         ns = sp[t + 1] - s0;
         if (ns == 1) return;      // finalised by the attention kernel
         if (ns > 1 && (int64_t)s0 + ns > kp.ws_capacity_splits) {
-            if (tid == 0) set_status(kp, SFM_STATUS_WORKSPACE_OVERFLOW);
+            if (lane == 0) set_status(kp, SFM_STATUS_WORKSPACE_OVERFLOW);
             ns = 0;
         }
     }
-    for (int h = 0; h < kp.q_n; ++h) {
-        const int64_t row = (int64_t)t * kp.q_n + h;
-        uint16_t *o = reinterpret_cast<uint16_t *>(kp.out) + row * 512;
-        if (ns == 0) {
-            o[tid] = to_half(0.f, kp.dtype);
-            o[tid + 256] = to_half(0.f, kp.dtype);
-            if (tid == 0 && kp.lse) kp.lse[row] = -INFINITY;
-            continue;
-        }
-        // LSE of the row: max then sum over the splits (thread 0, split order)
-        __syncthreads();
-        if (tid == 0) {
-            float m = -INFINITY;
-            for (int s = 0; s < ns; ++s) m = fmaxf(m, kp.ws_lse[(int64_t)(s0 + s) * kp.q_n + h]);
-            float z = 0.f;
-            if (m != -INFINITY)
-                for (int s = 0; s < ns; ++s) z += expf(kp.ws_lse[(int64_t)(s0 + s) * kp.q_n + h] - m);
-            s_red[0] = m;
-            s_red[1] = z;
-        }
-        __syncthreads();
-        const float m = s_red[0], z = s_red[1];
-        const float L = m == -INFINITY ? -INFINITY : m + logf(z);
-        float a0 = 0.f, a1 = 0.f;
-        if (L != -INFINITY) {
-            float sink_f = 1.f;
-            if (kp.sinks) sink_f = 1.f / (1.f + expf(__ldg(kp.sinks + h) - L));
-            for (int c0 = 0; c0 < ns; c0 += kMaxSplits) {
-                const int cn = min(kMaxSplits, ns - c0);
-                __syncthreads();
-                if (tid < cn) s_w[tid] = expf(kp.ws_lse[(int64_t)(s0 + c0 + tid) * kp.q_n + h] - L);
-                __syncthreads();
-                for (int s = 0; s < cn; ++s) {
-                    const float *os = kp.ws_o + ((int64_t)(s0 + c0 + s) * kp.q_n + h) * 512;
-                    a0 = fmaf(s_w[s], os[tid], a0);
-                    a1 = fmaf(s_w[s], os[tid + 256], a1);
+    const int64_t row = (int64_t)t * kp.q_n + h;
+    // LSE of the row over its splits: lane s holds split s (in chunks of 32)
+    float m = -INFINITY;
+    for (int c = 0; c < ns; c += 32)
+        if (c + lane < ns) m = fmaxf(m, kp.ws_lse[(int64_t)(s0 + c + lane) * kp.q_n + h]);
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    float z = 0.f;
+    if (m != -INFINITY)
+        for (int c = 0; c < ns; c += 32)
+            if (c + lane < ns) z += expf(kp.ws_lse[(int64_t)(s0 + c + lane) * kp.q_n + h] - m);
+    for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+    const float L = m == -INFINITY ? -INFINITY : m + logf(z);
+    float acc[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) acc[j] = 0.f;
+    if (L != -INFINITY) {
+        for (int c = 0; c < ns; c += 32) {
+            const int cn = min(32, ns - c);
+            const float wl = lane < cn ? expf(kp.ws_lse[(int64_t)(s0 + c + lane) * kp.q_n + h] - L) : 0.f;
+            for (int s = 0; s < cn; ++s) {
+                const float w = __shfl_sync(0xffffffffu, wl, s);
+                const float4 *src = reinterpret_cast<const float4 *>(
+                    kp.ws_o + ((int64_t)(s0 + c + s) * kp.q_n + h) * 512 + lane * 16);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const float4 v = src[q];
+                    acc[4 * q + 0] = fmaf(w, v.x, acc[4 * q + 0]);
+                    acc[4 * q + 1] = fmaf(w, v.y, acc[4 * q + 1]);
+                    acc[4 * q + 2] = fmaf(w, v.z, acc[4 * q + 2]);
+                    acc[4 * q + 3] = fmaf(w, v.w, acc[4 * q + 3]);
                 }
             }
-            a0 *= sink_f;
-            a1 *= sink_f;
         }
-        o[tid] = to_half(a0, kp.dtype);
-        o[tid + 256] = to_half(a1, kp.dtype);
-        if (tid == 0 && kp.lse) kp.lse[row] = L;
+        if (kp.sinks) {
+            const float f = 1.f / (1.f + expf(__ldg(kp.sinks + h) - L));
+#pragma unroll
+            for (int j = 0; j < 16; ++j) acc[j] *= f;
+        }
     }
+    uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(kp.out) + row * 512 + lane * 16);
+    dst[0] = make_uint4(to_half2(acc[0], acc[1], kp.dtype), to_half2(acc[2], acc[3], kp.dtype),
+                        to_half2(acc[4], acc[5], kp.dtype), to_half2(acc[6], acc[7], kp.dtype));
+    dst[1] = make_uint4(to_half2(acc[8], acc[9], kp.dtype), to_half2(acc[10], acc[11], kp.dtype),
+                        to_half2(acc[12], acc[13], kp.dtype), to_half2(acc[14], acc[15], kp.dtype));
+    if (lane == 0 && kp.lse) kp.lse[row] = L;
 }
 
 __global__ void __launch_bounds__(256) sfm_debug_kernel(KParams kp)
@@ -119,7 +127,8 @@ __global__ void __launch_bounds__(256) sfm_debug_kernel(KParams kp)
 cudaError_t launch_combine(const KParams &kp, cudaStream_t st)
 {
     if (kp.T == 0) return cudaSuccess;
-    sfm_combine_kernel<<<kp.T, kThreads, 0, st>>>(kp);
+    dim3 grid(kp.T, (kp.q_n + kHeadsPerBlock - 1) / kHeadsPerBlock);
+    sfm_combine_kernel<<<grid, kThreads, 0, st>>>(kp);
     return cudaGetLastError();
 }
 

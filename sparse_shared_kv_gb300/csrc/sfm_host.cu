@@ -210,6 +210,7 @@ void fill_common(KParams &kp, const sfm_params &p, const Plan &pl)
     kp.split_rows = pl.split_rows;
     kp.path = pl.path;
     kp.fingerprint = (int32_t)fingerprint(p, pl);
+    kp.wcap = pl.T * pl.max_splits_per_token;
 }
 
 void fill_lengths(KParams &kp, const sfm_tensors &t)
@@ -293,7 +294,7 @@ int sfm_metadata_size(const sfm_params *params, size_t *n_int32)
     Plan pl;
     rc = make_plan(*params, &pl);
     if (rc) return rc;
-    *n_int32 = (size_t)meta_words(pl.G, (int)pl.T);
+    *n_int32 = (size_t)meta_words(pl.G, (int)pl.T, pl.T * pl.max_splits_per_token);
     return SFM_OK;
 }
 
@@ -320,7 +321,7 @@ int sfm_metadata(const sfm_params *params, const sfm_tensors *lengths, int32_t *
     Plan pl;
     rc = make_plan(*params, &pl);
     if (rc) return rc;
-    if (metadata_n < (size_t)meta_words(pl.G, (int)pl.T)) return SFM_ERR_WORKSPACE;
+    if (metadata_n < (size_t)meta_words(pl.G, (int)pl.T, pl.T * pl.max_splits_per_token)) return SFM_ERR_WORKSPACE;
     KParams kp;
     fill_common(kp, *params, pl);
     fill_lengths(kp, *lengths);
@@ -344,7 +345,7 @@ int sfm_forward(const sfm_params *params, const sfm_tensors *in, const int32_t *
     Plan pl;
     rc = make_plan(p, &pl);
     if (rc) return rc;
-    if (metadata_n < (size_t)meta_words(pl.G, (int)pl.T)) return SFM_ERR_WORKSPACE;
+    if (metadata_n < (size_t)meta_words(pl.G, (int)pl.T, pl.T * pl.max_splits_per_token)) return SFM_ERR_WORKSPACE;
     const size_t need = workspace_bytes_for(p, pl);
     if (workspace_bytes < need || (need && !workspace) || ((uintptr_t)workspace & 255u)) return SFM_ERR_WORKSPACE;
 

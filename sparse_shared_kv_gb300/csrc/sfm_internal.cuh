@@ -18,26 +18,33 @@ namespace sfm {
 
 // ----------------------------------------------------------------------------
 // metadata layout (int32 words)
-//   [0, HDR)                      header (H_* below)
-//   [HDR, HDR+G+1)                worker split ranges: worker c owns splits [ws[c], ws[c+1])
-//   [.., +T+1)                    split prefix per query row: row t owns splits [sp[t], sp[t+1])
-//   [.., +T+1)                    cost prefix per query row (attended rows + per-split overhead)
+//   [0, HDR)                  header (H_* below)
+//   ws[G + 1]                 worker split ranges: worker c owns splits [ws[c], ws[c+1])
+//   sp[T + 1]                 split prefix per query row: row t owns splits [sp[t], sp[t+1])
+//   cp[T + 1]                 cost prefix per query row (attended rows + per-split overhead)
+//   rec[T][8]                 per query row: b, kv_len, cmp_len, p_cmp, lo, hi, n_ori, n_cmp
+//   own[Wcap]                 owning query row of every split
 // ----------------------------------------------------------------------------
 constexpr int32_t kMetaMagic = 0x53464d31;   // "SFM1"
 constexpr int kHdr = 16;
+constexpr int kRecWords = 8;
 enum MetaHeader {
     H_MAGIC = 0, H_FPRINT = 1, H_TOKENS = 2, H_WORKERS = 3, H_SPLIT = 4, H_PATH = 5,
-    H_TOTAL_SPLITS = 6, H_FLAGS = 7
+    H_TOTAL_SPLITS = 6, H_FLAGS = 7, H_LENFLAGS = 8, H_WCAP = 9
 };
-// modelled cost of one split beyond its rows (Q load, partial write), in rows
-constexpr int kSplitOverheadRows = 32;
+// modelled cost of one split beyond its rows, in rows: a split pays the
+// latency of its metadata / Q / first-tile loads and of its epilogue
+// whatever its length, so splits are balanced first by count, then by rows
+constexpr int kSplitOverheadRows = 128;
 
 __host__ __device__ inline int64_t meta_ws_off() { return kHdr; }
 __host__ __device__ inline int64_t meta_split_off(int G) { return kHdr + (int64_t)G + 1; }
 __host__ __device__ inline int64_t meta_cost_off(int G, int T) { return kHdr + (int64_t)G + 1 + (int64_t)T + 1; }
-__host__ __device__ inline int64_t meta_words(int G, int T)
+__host__ __device__ inline int64_t meta_rec_off(int G, int T) { return meta_cost_off(G, T) + (int64_t)T + 1; }
+__host__ __device__ inline int64_t meta_own_off(int G, int T) { return meta_rec_off(G, T) + (int64_t)kRecWords * T; }
+__host__ __device__ inline int64_t meta_words(int G, int T, int64_t wcap)
 {
-    int64_t n = kHdr + (int64_t)G + 1 + 2 * ((int64_t)T + 1);
+    int64_t n = meta_own_off(G, T) + wcap;
     return n < 1024 ? 1024 : n;
 }
 
@@ -61,6 +68,7 @@ struct KParams {
     // plan
     int32_t G, split_rows, fingerprint, path;
     int64_t ws_capacity_splits;
+    int64_t wcap;                           // capacity of the split -> row map
     // tensors
     const void *q;
     const uint8_t *ori_kv, *cmp_kv;

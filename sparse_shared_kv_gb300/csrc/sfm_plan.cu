@@ -53,8 +53,15 @@ __global__ void __launch_bounds__(kPlanThreads) sfm_plan_kernel(KParams kp)
     int32_t *ws = meta + meta_ws_off();
     int32_t *sp = meta + meta_split_off(G);
     int32_t *cp = meta + meta_cost_off(G, T);
+    int32_t *rec = meta + meta_rec_off(G, T);
+    int32_t *own = meta + meta_own_off(G, T);
     const int tid = threadIdx.x;
-    if (tid == 0) s_overflow = 0;
+    if (tid == 0) {
+        s_overflow = 0;
+        meta[H_LENFLAGS] = 0;       // length problems found while planning are OR-ed here
+    }
+    __syncthreads();
+    kp.status = meta + H_LENFLAGS;
 
     // 1. per-row split count and cost; each thread owns a contiguous run of rows
     const int per = (T + kPlanThreads - 1) / kPlanThreads;
@@ -74,9 +81,19 @@ __global__ void __launch_bounds__(kPlanThreads) sfm_plan_kernel(KParams kp)
         const Tok k = token_info(kp, t);
         const int64_t n = (int64_t)k.n_ori + k.n_cmp;
         const int64_t ns = n > 0 ? (n + S - 1) / S : 0;
-        if (ex_s > INT32_MAX || ex_c > INT32_MAX) s_overflow = 1;
+        if (ex_s > INT32_MAX || ex_c > INT32_MAX || ex_s + ns > kp.wcap) s_overflow = 1;
         sp[t] = (int32_t)ex_s;
         cp[t] = (int32_t)ex_c;
+        int32_t *r = rec + (int64_t)kRecWords * t;
+        r[0] = k.b;
+        r[1] = k.kv_len;
+        r[2] = k.cmp_len;
+        r[3] = k.p_cmp;
+        r[4] = k.lo;
+        r[5] = k.hi;
+        r[6] = k.n_ori;
+        r[7] = k.n_cmp;
+        for (int64_t j = 0; j < ns && ex_s + j < kp.wcap; ++j) own[ex_s + j] = t;
         ex_s += ns;
         ex_c += n + ns * kSplitOverheadRows;
     }
@@ -125,7 +142,8 @@ __global__ void __launch_bounds__(kPlanThreads) sfm_plan_kernel(KParams kp)
         meta[H_PATH] = kp.path;
         meta[H_TOTAL_SPLITS] = W;
         meta[H_FLAGS] = s_overflow ? SFM_STATUS_PLAN_OVERFLOW : 0;
-        for (int j = 8; j < kHdr; ++j) meta[j] = 0;
+        meta[H_WCAP] = (int32_t)(kp.wcap < INT32_MAX ? kp.wcap : INT32_MAX);
+        for (int j = 10; j < kHdr; ++j) meta[j] = 0;
     }
 }
 
