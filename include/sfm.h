@@ -23,8 +23,9 @@
  *           cmp_sparse_indices (-1 = invalid, valid entries first).
  *
  * with p = kv_len - q_len + i for query row i (right-down alignment, CP切分示例)
- * and p_cmp = cmp_len * cmp_ratio + cmp_residual_kv - q_len + i (cmp_residual_kv
- * "用于恢复cmp侧mask长度"; equal to p under the documented contract).
+ * and p_cmp = cmp_len * cmp_ratio + cmp_residual_kv - q_len + i (参数说明: the
+ * residual recovers the cmp-side mask length; equal to p under the documented
+ * contract).
  * Optional per-head fp32 sinks add exp(sink - m) to the softmax denominator
  * only; the LSE excludes them.  An empty attended set gives O = 0 and
  * LSE = -inf.
@@ -149,7 +150,7 @@ typedef struct sfm_params {
  *   cmp_residual_kv      (b) int32, 0 <= r < cmp_ratio (required when cmp_mask_mode = 3)
  *   sinks                (q_n) fp32 or NULL
  * Row strides are in bytes, >= the row size and a multiple of 16 (rows may be
- * padded: "ori_kv和cmp_kv允许存在行间padding"); *_rows is the number of rows
+ * padded between rows, 公共参数组); *_rows is the number of rows
  * the buffer holds (used to bounds-check every resolved row).  Base pointers
  * must be 16-byte aligned. */
 typedef struct sfm_tensors {

@@ -30,9 +30,10 @@
  *     (-1 = invalid, valid first) ("sparse_flash_mla" doc, 功能说明: SWA / CSA
  *     / HCA; 参数说明: cmp_sparse_indices, cmp_residual_kv).
  * Query row i of batch b sits at p = kv_len - q_len + i (right-down
- * alignment; "sparse_flash_mla" doc, CP切分示例: "kernel推导出的q起点").
+ * alignment; "sparse_flash_mla" doc, CP切分示例: the q start the kernel
+ * derives is the prefix length minus the query length).
  * The cmp side uses the pre-compression length cmp_len*cmp_ratio + residual
- * ("cmp_residual_kv ... 用于恢复cmp侧mask长度"), so p_cmp = that length -
+ * (参数说明: the residual recovers the cmp-side mask length), so p_cmp = that length -
  * q_len + i; under the documented contract it equals p.
  *
  * Readings taken where the pages are silent (each listed in the design notes):

@@ -4,7 +4,8 @@
 // doc (zh), 约束说明 / 参数组约束: kv_n = 1, d = 512, q_n in 1..128, the
 // SWA / CSA / HCA attribute combinations of 计算模式参数组, the layout pairs of
 // the layout匹配关系表 and the paged block-size rule.  Tensor values are not
-// read here (用户保证); the kernels bounds-check them instead.
+// read here (the pages leave their validity to the caller); the kernels
+// bounds-check them instead.
 #include <math.h>
 #include <string.h>
 
@@ -239,7 +240,7 @@ int validate_tensors(const sfm_params &p, const sfm_tensors *t)
         if (!aligned16(t->cmp_kv)) return SFM_ERR_LAYOUT;
         if (t->cmp_row_stride < rb || t->cmp_row_stride % 16 || t->cmp_rows <= 0) return SFM_ERR_LAYOUT;
     } else if (t->cmp_kv || t->cmp_sparse_indices || t->cmp_block_table) {
-        return SFM_ERR_INVALID_ARG;   // SWA: 不传cmp_kv、cmp_sparse_indices和cmp_block_table
+        return SFM_ERR_INVALID_ARG;   // SWA takes no cmp tensors (计算模式参数组)
     }
     if (p.cmp_topk > 0 && !t->cmp_sparse_indices) return SFM_ERR_INVALID_ARG;
     if (p.has_cmp_kv && p.cmp_topk == 0 && t->cmp_sparse_indices) return SFM_ERR_INVALID_ARG;  // HCA

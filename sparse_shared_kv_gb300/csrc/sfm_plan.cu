@@ -7,7 +7,7 @@
 //   * per query row t: its attended-position count n_t cut into
 //     ceil(n_t / split_rows) splits -- a function of the row's own count and
 //     the params only, so a row's arithmetic never depends on the rest of the
-//     batch ("确定性计算: 默认支持 batch invariance");
+//     batch (the 确定性计算 section makes batch invariance the default);
 //   * per worker (persistent CTA or CTA pair): a contiguous range of splits
 //     chosen so that every worker gets about the same modelled cost
 //     (attended rows + a fixed per-split overhead).
