@@ -207,6 +207,36 @@ int sfm_forward(const sfm_params *params, const sfm_tensors *inputs, const int32
                 float softmax_scale, void *out, float *lse, void *workspace, size_t workspace_bytes,
                 int32_t *status, sfm_stream_t stream);
 
+/* Size of the fixed device workspace used by sfm_forward_noalloc(): 32 MiB. */
+#define SFM_NOALLOC_WORKSPACE_BYTES ((size_t)32 << 20)
+
+/* sfm_forward() for callers that cannot allocate device memory.  The pages
+ * have no counterpart to this entry point; it exists because some callers of
+ * this library cannot call cudaMalloc when they run attention -- a graph
+ * replayed with its memory frozen, a plug-in whose host framework owns every
+ * allocation, a latency-critical path that must not allocate -- yet
+ * sfm_forward() needs sfm_workspace_size() bytes of scratch for split-KV
+ * partial results.
+ *
+ * Same arguments and behaviour as sfm_forward() minus the workspace: the
+ * scratch comes from a fixed SFM_NOALLOC_WORKSPACE_BYTES device array that is
+ * part of the library's module (every GPU that loads the module keeps it
+ * until the process exits).  Nothing is allocated by this call: no cudaMalloc,
+ * no cudaFree, no allocating library routine.  The caller still owns and
+ * passes the inputs, the metadata, out, lse and status.
+ *   - Returns SFM_ERR_WORKSPACE, enqueuing nothing, when these params need
+ *     more than SFM_NOALLOC_WORKSPACE_BYTES of workspace.
+ *   - The first call that needs scratch on a device looks up the array's
+ *     device address (cudaGetSymbolAddress) once for that device; make that
+ *     first call before any stream capture.
+ *   - All calls on a device share the array and it keeps the last call's
+ *     contents: calls whose kernels may overlap on the GPU (unordered
+ *     streams) race on it.  Every scratch word is written before it is read
+ *     within a call, so nothing needs clearing between calls. */
+int sfm_forward_noalloc(const sfm_params *params, const sfm_tensors *inputs, const int32_t *metadata,
+                        size_t metadata_n, float softmax_scale, void *out, float *lse, int32_t *status,
+                        sfm_stream_t stream);
+
 /* Test hook: the rows the kernels resolve for every query row.  For token t
  * and attended position k < counts[t] (ori positions first, then cmp),
  * rows[t * cap + k] = -1 for a skipped entry, else the logical index

@@ -65,8 +65,9 @@ class SfmTensors(C.Structure):
     ]
 
 
-EXPORTS = ("sfm_metadata_size", "sfm_workspace_size", "sfm_metadata", "sfm_forward", "sfm_debug_attended",
-           "sfm_set_profile_events", "sfm_error_string", "sfm_abi_version")
+EXPORTS = ("sfm_metadata_size", "sfm_workspace_size", "sfm_metadata", "sfm_forward", "sfm_forward_noalloc",
+           "sfm_debug_attended", "sfm_set_profile_events", "sfm_error_string", "sfm_abi_version")
+NOALLOC_WORKSPACE_BYTES = 32 << 20
 
 _lib = None
 
@@ -89,12 +90,14 @@ def lib():
         l.sfm_metadata.argtypes = [P, T, C.c_void_p, C.c_size_t, C.c_void_p]
         l.sfm_forward.argtypes = [P, T, C.c_void_p, C.c_size_t, C.c_float, C.c_void_p, C.c_void_p, C.c_void_p,
                                   C.c_size_t, C.c_void_p, C.c_void_p]
+        l.sfm_forward_noalloc.argtypes = [P, T, C.c_void_p, C.c_size_t, C.c_float, C.c_void_p, C.c_void_p,
+                                          C.c_void_p, C.c_void_p]
         l.sfm_debug_attended.argtypes = [P, T, C.c_void_p, C.c_int64, C.c_void_p, C.c_void_p, C.c_void_p]
         l.sfm_set_profile_events.argtypes = [C.c_void_p, C.c_void_p]
         l.sfm_error_string.argtypes = [C.c_int]
         l.sfm_error_string.restype = C.c_char_p
-        for n in ("sfm_metadata_size", "sfm_workspace_size", "sfm_metadata", "sfm_forward", "sfm_debug_attended",
-                  "sfm_set_profile_events", "sfm_abi_version"):
+        for n in ("sfm_metadata_size", "sfm_workspace_size", "sfm_metadata", "sfm_forward", "sfm_forward_noalloc",
+                  "sfm_debug_attended", "sfm_set_profile_events", "sfm_abi_version"):
             getattr(l, n).restype = C.c_int
         _lib = l
     return _lib
@@ -170,6 +173,15 @@ def sfm_forward(params: SfmParams, tensors: SfmTensors, metadata: torch.Tensor, 
     _check("sfm_forward", lib().sfm_forward(
         C.byref(params), C.byref(tensors), metadata.data_ptr(), metadata.numel(), C.c_float(softmax_scale),
         out.data_ptr(), _ptr(lse), _ptr(workspace), ws_bytes, _ptr(status), _stream(stream)))
+
+
+def sfm_forward_noalloc(params: SfmParams, tensors: SfmTensors, metadata: torch.Tensor, softmax_scale: float,
+                        out: torch.Tensor, lse: Optional[torch.Tensor], status: Optional[torch.Tensor] = None,
+                        stream=None) -> None:
+    """sfm_forward with the library's fixed device workspace (no allocation)."""
+    _check("sfm_forward_noalloc", lib().sfm_forward_noalloc(
+        C.byref(params), C.byref(tensors), metadata.data_ptr(), metadata.numel(), C.c_float(softmax_scale),
+        out.data_ptr(), _ptr(lse), _ptr(status), _stream(stream)))
 
 
 def sfm_debug_attended(params: SfmParams, tensors: SfmTensors, rows: torch.Tensor, cap: int,
