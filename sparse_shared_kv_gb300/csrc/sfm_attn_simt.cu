@@ -130,6 +130,8 @@ __global__ void __launch_bounds__(kThreads) sfm_attn_simt_kernel(KParams kp)
 {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     Smem &s = *reinterpret_cast<Smem *>(smem_raw);
+    grid_launch_dependents();
+    grid_dependency_wait();      // the plan comes from the preceding planner launch
     if (!meta_ok(kp)) return;   // the combine kernel zeroes the outputs and flags the status
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -272,8 +274,7 @@ cudaError_t launch_attn_simt(const KParams &kp, cudaStream_t st)
                                          (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid(kp.G, (kp.q_n + HG - 1) / HG);
-    sfm_attn_simt_kernel<<<grid, kThreads, smem, st>>>(kp);
-    return cudaGetLastError();
+    return launch_dependent(sfm_attn_simt_kernel, grid, dim3(kThreads), smem, st, kp);
 }
 
 }  // namespace sfm

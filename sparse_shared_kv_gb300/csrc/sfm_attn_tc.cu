@@ -1,7 +1,9 @@
-// sfm_attn_tc.cu -- tensor-core (tcgen05 / TMEM) split-KV attention for up
-// to 64 query heads with plain bf16 / fp16 KV rows.
+// sfm_attn_tc.cu -- tensor-core (tcgen05 / TMEM) split-KV attention for
+// plain bf16 / fp16 KV rows.
 //
-// One persistent CTA per SM walks the splits the planner gave its worker.
+// One persistent CTA per SM walks the work units the planner gave its worker;
+// a unit is one split for one group of up to 64 query heads (128 heads make
+// two units per split, whose second pass over the split's rows hits L2).
 // Per 64-row KV tile of a split:
 //   producer warps 0-1   resolve the attended rows (window / compressed /
 //                        indices through the block tables) and stream each
@@ -57,7 +59,7 @@ constexpr float kRescaleThreshold = 8.0f;    // log2 units
 // barrier slots (8 bytes each) at MISC_OFF
 enum Bar {
     B_KV_FULL = 0, B_KV_EMPTY = 2, B_S_FULL = 4, B_S_FREE = 6, B_P_FULL = 8, B_O_DONE = 9, B_Q_FULL = 10,
-    B_Q_EMPTY = 11, B_O_FREE = 12, B_TEARDOWN = 13, B_SM_SYNC = 14, kNumBars = 15
+    B_Q_EMPTY = 11, B_O_FREE = 12, B_TEARDOWN = 13, B_ALPHA = 14, B_STATS = 16, kNumBars = 17
 };
 constexpr uint32_t TMEM_SLOT_OFF = MISC_OFF + 128;
 constexpr uint32_t ABORT_OFF = MISC_OFF + 132;
@@ -124,15 +126,15 @@ __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(KParams kp)
     float *stats_s = reinterpret_cast<float *>(base + STATS_OFF);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const bool ok = meta_ok(kp);
     const bool bf16 = kp.dtype == SFM_DTYPE_BF16;
+    grid_launch_dependents();    // the combine kernel may launch; it waits for this grid
 
     // ---------------- set-up ----------------
     for (uint32_t i = tid; i < 24576u / 16u; i += kThreads)
         reinterpret_cast<uint4 *>(base + P_OFF)[i] = make_uint4(0, 0, 0, 0);
     if (tid == 0) {
-        mbar_init(bar(B_KV_FULL + 0), 64);
-        mbar_init(bar(B_KV_FULL + 1), 64);
+        mbar_init(bar(B_KV_FULL + 0), 66);   // 64 copy-completion arrivals + 2 row-mask words
+        mbar_init(bar(B_KV_FULL + 1), 66);
         mbar_init(bar(B_KV_EMPTY + 0), 1);
         mbar_init(bar(B_KV_EMPTY + 1), 1);
         mbar_init(bar(B_S_FULL + 0), 1);
@@ -145,7 +147,9 @@ __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(KParams kp)
         mbar_init(bar(B_Q_EMPTY), 1);
         mbar_init(bar(B_O_FREE), 128);
         mbar_init(bar(B_TEARDOWN), 1);
-        mbar_init(bar(B_SM_SYNC), 128);
+        mbar_init(bar(B_ALPHA + 0), 64);
+        mbar_init(bar(B_ALPHA + 1), 64);
+        mbar_init(bar(B_STATS), 64);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -159,6 +163,9 @@ __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(KParams kp)
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(base + TMEM_SLOT_OFF);
 
+    // everything above overlapped the planner; the plan is read from here on
+    grid_dependency_wait();
+    const bool ok = meta_ok(kp);
     const int worker = blockIdx.x;
     const int32_t *sp = kp.meta + meta_split_off(kp.G);
     const int w_beg = ok ? kp.meta[meta_ws_off() + worker] : 0;
@@ -166,81 +173,80 @@ __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(KParams kp)
 
     if (warp < 2) {
         // ======================= producer =======================
-        const int pt = tid;                 // tile row / Q head handled by this thread
-        uint32_t pend_bar[3];
-        int pend = 0;
-        auto flush_one = [&]() {
-            if (pend >= 3) cp_async_wait<2>();
-            else if (pend == 2) cp_async_wait<1>();
-            else cp_async_wait<0>();
-            fence_proxy_async_smem();
-            mbar_arrive(pend_bar[0]);
-            pend_bar[0] = pend_bar[1];
-            pend_bar[1] = pend_bar[2];
-            --pend;
-        };
+        // Thread pt owns tile row pt (and Q head row pt).  Copies arrive on the
+        // stage barrier by themselves when they land (cp.async.mbarrier), so
+        // the producer never waits for its own loads; it only waits for a
+        // free stage.  Rows are resolved one tile ahead of the tile in flight.
+        const int pt = tid;
         const uint8_t *zero_src = static_cast<const uint8_t *>(kp.q);
         int g = 0, ks = 0;
         bool stop = false;
-        for (int w = w_beg; w < w_end && !stop; ++w) {
+        for (int u = w_beg; u < w_end && !stop; ++u) {
+            const int w = u / kp.head_groups, h0 = (u - w * kp.head_groups) * 64;
+            const int nh = min(64, kp.q_n - h0);
             const SplitInfo s = split_info(kp, sp, w);
-            // Q of the query row (all 64 head rows; heads >= q_n are zero)
-            while (pend) flush_one();
             if (ks > 0 && !warp_wait(bar(B_Q_EMPTY), (ks - 1) & 1, abort_flag)) break;
-            __syncwarp();
             {
-                const bool live = pt < kp.q_n;
-                const uint8_t *src = live ? static_cast<const uint8_t *>(kp.q) +
-                                                ((int64_t)s.t * kp.q_n + pt) * 1024
-                                          : zero_src;
-                for (int C = 0; C < 64; ++C) {
-                    const uint32_t dst = sb + Q_OFF + (C >> 3) * 8192u + sw128(pt, C & 7);
-                    cp_async16(dst, live ? src + C * 16 : zero_src, live ? 16u : 0u);
+                // Q rows of this warp's 32 heads, one 1 KB row per step: lane L
+                // copies 16-byte chunks L and L + 32 (512 contiguous bytes per
+                // instruction)
+                const uint8_t *qrow = static_cast<const uint8_t *>(kp.q) + ((int64_t)s.t * kp.q_n + h0) * 1024;
+                for (int rr = 0; rr < 32; ++rr) {
+                    const int hh = warp * 32 + rr;
+                    const bool live = hh < nh;
+#pragma unroll
+                    for (int half = 0; half < 2; ++half) {
+                        const int C = lane + half * 32;
+                        const uint32_t dst = sb + Q_OFF + (C >> 3) * 8192u + sw128(hh, C & 7);
+                        cp_async16(dst, live ? qrow + (int64_t)hh * 1024 + C * 16 : zero_src, live ? 16u : 0u);
+                    }
                 }
-                cp_async_commit();
-                pend_bar[pend++] = bar(B_Q_FULL);
+                cp_async_arrive_noinc(bar(B_Q_FULL));
             }
-            // rows of tile 0 resolve while Q streams in; tile i+1 resolves while
-            // tile i streams in and while waiting for a free stage
             auto resolve = [&](int i) -> const uint8_t * {
                 const int pos = s.pos0 + i * NT + pt;
                 if (pos >= s.pos1) return nullptr;
                 int logical, src;
                 return resolve_row(kp, s.k, s.t, pos, &logical, &src);
             };
-            const uint8_t *rp = resolve(0);
-            const uint8_t *rp_next = s.ntiles > 1 ? resolve(1) : nullptr;   // independent chains overlap
+            const uint8_t *rp[2];
+            rp[0] = resolve(0);
+            rp[1] = s.ntiles > 1 ? resolve(1) : nullptr;      // independent chains overlap
             for (int i = 0; i < s.ntiles; ++i, ++g) {
                 const int st = g & 1, use = g >> 1;
-                if (use >= 1) {
-                    // never block while holding copies whose arrival is deferred:
-                    // the MMA warp may be waiting for exactly those rows
-                    const bool ready = __all_sync(0xffffffffu, mbar_test(bar(B_KV_EMPTY + st), (use - 1) & 1));
-                    if (!ready) {
-                        while (pend) flush_one();
-                        if (!warp_wait(bar(B_KV_EMPTY + st), (use - 1) & 1, abort_flag)) {
-                            stop = true;
-                            break;
-                        }
+                if (use >= 1 && !warp_wait(bar(B_KV_EMPTY + st), (use - 1) & 1, abort_flag)) {
+                    stop = true;
+                    break;
+                }
+                const uint8_t *row = rp[i & 1];
+                __syncwarp();
+                const uint32_t vm = __ballot_sync(0xffffffffu, row != nullptr);
+                const uint32_t stage = sb + KV_OFF + st * KV_STAGE;
+                // this warp's 32 tile rows, one row per step (pointer broadcast
+                // from the lane that resolved it): 512 contiguous bytes per
+                // warp instruction
+                const unsigned long long my_row = reinterpret_cast<unsigned long long>(row);
+                for (int rr = 0; rr < 32; ++rr) {
+                    const uint8_t *src = reinterpret_cast<const uint8_t *>(__shfl_sync(0xffffffffu, my_row, rr));
+                    const int tr = warp * 32 + rr;
+#pragma unroll
+                    for (int half = 0; half < 2; ++half) {
+                        const int C = lane + half * 32;
+                        const uint32_t dst = stage + (C >> 3) * 8192u + sw128(tr, C & 7);
+                        cp_async16(dst, src ? src + C * 16 : zero_src, src ? 16u : 0u);
                     }
                 }
-                __syncwarp();
-                const uint32_t vm = __ballot_sync(0xffffffffu, rp != nullptr);
-                if (lane == 0) valid_s[st * 2 + warp] = vm;
-                const uint32_t stage = sb + KV_OFF + st * KV_STAGE;
-                for (int C = 0; C < 64; ++C) {
-                    const uint32_t dst = stage + (C >> 3) * 8192u + sw128(pt, C & 7);
-                    cp_async16(dst, rp ? rp + C * 16 : zero_src, rp ? 16u : 0u);
+                cp_async_arrive_noinc(bar(B_KV_FULL + st));
+                if (lane == 0) {
+                    valid_s[st * 2 + warp] = vm;          // this warp's 32 row-valid bits
+                    mbar_arrive(bar(B_KV_FULL + st));     // release: the word is visible with the phase
                 }
-                cp_async_commit();
-                pend_bar[pend++] = bar(B_KV_FULL + st);
-                rp = rp_next;
-                rp_next = i + 2 < s.ntiles ? resolve(i + 2) : nullptr;
-                while (pend > 1) flush_one();
+                // the next tile was resolved earlier; resolve the one after it now,
+                // behind the copies in flight
+                if (i >= 1 && i + 1 < s.ntiles) rp[(i + 1) & 1] = resolve(i + 1);
             }
             ++ks;
         }
-        while (pend) flush_one();
         cp_async_wait<0>();
     } else if (warp == 2) {
         // ======================= MMA issuer =======================
@@ -252,9 +258,11 @@ __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(KParams kp)
             const uint32_t id_pv = idesc_f16(128, 256, bf16, false, true);
             int g = 0, ks = 0;
             bool stop = false;
-            for (int w = w_beg; w < w_end && !stop; ++w) {
+            for (int u = w_beg; u < w_end && !stop; ++u) {
+                const int w = u / kp.head_groups;
                 const SplitInfo s = split_info(kp, sp, w);
                 if (!mbar_wait(bar(B_Q_FULL), ks & 1, abort_flag)) break;
+                fence_proxy_async_smem();       // cp.async (generic proxy) writes -> tensor-core reads
                 tc_fence_after();
                 int ns = 0, npv = 0;             // next tile to issue S / P.V for
                 uint64_t t_idle = 0;
@@ -264,6 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(KParams kp)
                         const int gi = g + ns, st = gi & 1;
                         if (mbar_test(bar(B_KV_FULL + st), (gi >> 1) & 1) &&
                             (gi < 2 || mbar_test(bar(B_S_FREE + st), ((gi >> 1) - 1) & 1))) {
+                            fence_proxy_async_smem();
                             tc_fence_after();
                             const uint32_t d = tmem + TM_S + st * 64;
                             const uint32_t kv = sb + KV_OFF + st * KV_STAGE;
@@ -324,18 +333,21 @@ __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(KParams kp)
         __syncwarp();
     } else if (warp >= 4) {
         // ======================= softmax / epilogue =======================
+        // Warps 4-5 own the score rows (heads) and O[:, 0:256]; warps 6-7 own
+        // O[:, 256:512] of the same heads.  Warps 4-5 publish each tile's
+        // rescale factor and the final (max, sum) through one-way mbarriers;
+        // only warps 6-7 wait on them.
         const int r = tid - 128;             // TMEM lane == score row
         const bool head_row = r < 64;
         const int h = r & 63;
         const uint32_t lane_base = static_cast<uint32_t>((warp - 4) * 32) << 16;
         const float sl2 = kp.scale_log2;
+        // epilogue staging: 2 KB per warp in P rows 64..127 (idle during the epilogue)
+        uint8_t *stage = base + P_OFF + 8192u + static_cast<uint32_t>(warp - 4) * 2048u;
         int g = 0, ks = 0;
-        uint32_t nsync = 0;                  // uses of the softmax-group barrier
-        auto group_sync = [&]() -> bool {
-            mbar_arrive(bar(B_SM_SYNC));
-            return warp_wait(bar(B_SM_SYNC), (nsync++) & 1, abort_flag);
-        };
-        for (int w = w_beg; w < w_end; ++w) {
+        for (int u = w_beg; u < w_end; ++u) {
+            const int w = u / kp.head_groups, h0 = (u - w * kp.head_groups) * 64;
+            const int nh = min(64, kp.q_n - h0);
             const SplitInfo s = split_info(kp, sp, w);
             float m = -INFINITY, l = 0.f;
             bool stop = false;
@@ -343,59 +355,89 @@ __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(KParams kp)
                 const int gi = g + i, st = gi & 1;
                 if (!warp_wait(bar(B_S_FULL + st), (gi >> 1) & 1, abort_flag)) { stop = true; break; }
                 tc_fence_after();
-                uint32_t sv[64];
-                if (warp < 6) {
+                float alpha = 1.f;
+                uint32_t pw[32];
+                const bool live_head = head_row && h < nh;
+                if (head_row) {
+                    uint32_t sv[64];
                     tmem_ld32(tmem + lane_base + TM_S + st * 64, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
                     tmem_ld32(tmem + lane_base + TM_S + st * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
                     tmem_wait_ld();
-                }
-                tc_fence_before();
-                mbar_arrive(bar(B_S_FREE + st));
-                if (!warp_wait(bar(B_KV_FULL + st), (gi >> 1) & 1, abort_flag)) { stop = true; break; }
-                float alpha = 1.f;
-                uint32_t pw[32];
-                const bool live_head = head_row && h < kp.q_n;
-                if (live_head) {
-                    const uint32_t v0 = valid_s[st * 2 + 0], v1 = valid_s[st * 2 + 1];
-                    float x[64];
-                    float tmax = -INFINITY;
+                    tc_fence_before();
+                    mbar_arrive(bar(B_S_FREE + st));
+                    if (!warp_wait(bar(B_KV_FULL + st), (gi >> 1) & 1, abort_flag)) { stop = true; break; }
+                    if (live_head) {
+                        const uint32_t v0 = valid_s[st * 2 + 0], v1 = valid_s[st * 2 + 1];
+                        float x[64];
 #pragma unroll
-                    for (int j = 0; j < 64; ++j) {
-                        const bool v = ((j < 32 ? v0 >> j : v1 >> (j - 32)) & 1u) != 0;
-                        x[j] = v ? __uint_as_float(sv[j]) * sl2 : -INFINITY;
-                        tmax = fmaxf(tmax, x[j]);
-                    }
-                    if (tmax > m + kRescaleThreshold) {
-                        alpha = (m == -INFINITY) ? 0.f : exp2f(m - tmax);
-                        m = tmax;
-                    }
-                    float sum = 0.f;
+                        for (int j = 0; j < 64; ++j) x[j] = __uint_as_float(sv[j]);
+                        if ((v0 & v1) != 0xffffffffu) {
 #pragma unroll
-                    for (int j = 0; j < 64; j += 2) {
-                        const float p0 = (m == -INFINITY) ? 0.f : exp2f(x[j] - m);
-                        const float p1 = (m == -INFINITY) ? 0.f : exp2f(x[j + 1] - m);
-                        sum += p0 + p1;
-                        pw[j >> 1] = pack2(p0, p1, bf16);
+                            for (int j = 0; j < 64; ++j)
+                                if (!(((j < 32 ? v0 >> j : v1 >> (j - 32)) & 1u))) x[j] = -INFINITY;
+                        }
+                        float mx[32];
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) mx[j] = fmaxf(x[2 * j], x[2 * j + 1]);
+#pragma unroll
+                        for (int w2 = 16; w2 >= 1; w2 >>= 1)
+#pragma unroll
+                            for (int j = 0; j < w2; ++j) mx[j] = fmaxf(mx[j], mx[j + w2]);
+                        const float tmax = mx[0] * sl2;   // softmax_scale > 0 keeps the arg-max
+                        if (tmax > m + kRescaleThreshold) {
+                            alpha = (m == -INFINITY) ? 0.f : fast_exp2(m - tmax);
+                            m = tmax;
+                        }
+                        float ps[32];
+                        if (m == -INFINITY) {
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) {
+                                ps[j] = 0.f;
+                                pw[j] = 0u;
+                            }
+                        } else {
+                            const float nm = -m;
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) {
+                                const float p0 = fast_exp2(fmaf(x[2 * j], sl2, nm));
+                                const float p1 = fast_exp2(fmaf(x[2 * j + 1], sl2, nm));
+                                ps[j] = p0 + p1;
+                                pw[j] = pack2(p0, p1, bf16);
+                            }
+                        }
+#pragma unroll
+                        for (int w2 = 16; w2 >= 1; w2 >>= 1)
+#pragma unroll
+                            for (int j = 0; j < w2; ++j) ps[j] += ps[j + w2];
+                        l = l * alpha + ps[0];
                     }
-                    l = l * alpha + sum;
+                    alpha_s[(gi & 1) * 64 + r] = alpha;
+                    mbar_arrive(bar(B_ALPHA + (gi & 1)));
+                } else {
+                    tc_fence_before();
+                    mbar_arrive(bar(B_S_FREE + st));
+                    if (!warp_wait(bar(B_ALPHA + (gi & 1)), (gi >> 1) & 1, abort_flag)) { stop = true; break; }
+                    alpha = alpha_s[(gi & 1) * 64 + h];
                 }
-                if (head_row) alpha_s[(gi & 1) * 64 + r] = alpha;
-                if (!group_sync()) { stop = true; break; }
-                __syncwarp();
-                const float my_alpha = head_row ? alpha : alpha_s[(gi & 1) * 64 + h];
                 if (gi >= 1 && !warp_wait(bar(B_O_DONE), (gi - 1) & 1, abort_flag)) { stop = true; break; }
                 tc_fence_after();
-                if (i > 0 && __any_sync(0xffffffffu, my_alpha != 1.f)) {
+                if (i > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
                     for (int c = 0; c < 8; ++c) {
                         uint32_t o[32];
                         tmem_ld32(tmem + lane_base + TM_O + c * 32, o);
                         tmem_wait_ld();
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * my_alpha);
+                        for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
                         tmem_st32(tmem + lane_base + TM_O + c * 32, o);
                     }
                     tmem_wait_st();
+                }
+                // the previous split's epilogue staged O through P rows 64..127:
+                // all four warps must be done with it before a new P lands there
+                if (i == 0 && ks > 0 && head_row && !warp_wait(bar(B_O_FREE), (ks - 1) & 1, abort_flag)) {
+                    stop = true;
+                    break;
                 }
                 if (live_head) {
                     uint8_t *prow = base + P_OFF;
@@ -413,53 +455,91 @@ __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(KParams kp)
             const int gl = g + s.ntiles - 1;
             if (!warp_wait(bar(B_O_DONE), gl & 1, abort_flag)) break;
             tc_fence_after();
+            float mm = m, ll = l;
             if (head_row) {
                 stats_s[2 * r] = m;
                 stats_s[2 * r + 1] = l;
+                mbar_arrive(bar(B_STATS));
+            } else {
+                if (!warp_wait(bar(B_STATS), ks & 1, abort_flag)) break;
+                mm = stats_s[2 * h];
+                ll = stats_s[2 * h + 1];
             }
-            if (!group_sync()) break;
-            const float mm = stats_s[2 * h], ll = stats_s[2 * h + 1];
             const bool final_split = s.nsplit == 1;
-            const bool store = h < kp.q_n && (final_split || w < kp.ws_capacity_splits);
-            if (!final_split && w >= kp.ws_capacity_splits && r == 0) set_status(kp, SFM_STATUS_WORKSPACE_OVERFLOW);
+            const bool ws_ok = final_split || w < kp.ws_capacity_splits;
+            if (!ws_ok && r == 0) set_status(kp, SFM_STATUS_WORKSPACE_OVERFLOW);
             float inv = 0.f;
             if (ll > 0.f) {
                 float den = ll;
-                if (final_split && kp.sinks) den += exp2f(__ldg(kp.sinks + h) * 1.4426950408889634f - mm);
+                if (final_split && kp.sinks) den += exp2f(__ldg(kp.sinks + h0 + h) * 1.4426950408889634f - mm);
                 inv = 1.f / den;
             }
-            const int64_t row = (int64_t)s.t * kp.q_n + h;
-            const int dcol = head_row ? 0 : 256;
+            // Coalesced stores: each thread parks its row chunk in its warp's
+            // staging slice (64 B per row, 16-byte pieces rotated by row), then
+            // lane L writes piece L%4 of row 8k + L/4: a warp store covers
+            // eight whole 64-byte row segments.
+            const int wl = warp - 4;
+            const int srow = lane >> 2, spiece = lane & 3;
+            auto rd_row = [&](int k) { return k * 8 + srow; };          // local row read back by this lane
+            auto row_head = [&](int lr) { return (wl * 32 + lr) & 63; };
+            auto row_dcol = [&](int lr) { return (wl * 32 + lr) < 64 ? 0 : 256; };
+            if (final_split) {
+                uint16_t *obase = static_cast<uint16_t *>(kp.out) + ((int64_t)s.t * kp.q_n + h0) * 512;
 #pragma unroll 1
-            for (int c = 0; c < 8; ++c) {
-                uint32_t o[32];
-                __syncwarp();
-                tmem_ld32(tmem + lane_base + TM_O + c * 32, o);
-                tmem_wait_ld();
-                if (store && final_split) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(kp.out) + row * 512 + dcol + c * 32);
+                for (int c = 0; c < 8; ++c) {                    // 32 columns per chunk
+                    uint32_t o[32];
+                    __syncwarp();
+                    tmem_ld32(tmem + lane_base + TM_O + c * 32, o);
+                    tmem_wait_ld();
 #pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4) {
-                        const int j = q4 * 8;
-                        dst[q4] = make_uint4(pack2(__uint_as_float(o[j]) * inv, __uint_as_float(o[j + 1]) * inv, bf16),
-                                             pack2(__uint_as_float(o[j + 2]) * inv, __uint_as_float(o[j + 3]) * inv, bf16),
-                                             pack2(__uint_as_float(o[j + 4]) * inv, __uint_as_float(o[j + 5]) * inv, bf16),
-                                             pack2(__uint_as_float(o[j + 6]) * inv, __uint_as_float(o[j + 7]) * inv, bf16));
+                    for (int q = 0; q < 4; ++q) {
+                        const int j = q * 8;
+                        *reinterpret_cast<uint4 *>(stage + lane * 64 + ((q ^ (lane & 3)) << 4)) = make_uint4(
+                            pack2(__uint_as_float(o[j]) * inv, __uint_as_float(o[j + 1]) * inv, bf16),
+                            pack2(__uint_as_float(o[j + 2]) * inv, __uint_as_float(o[j + 3]) * inv, bf16),
+                            pack2(__uint_as_float(o[j + 4]) * inv, __uint_as_float(o[j + 5]) * inv, bf16),
+                            pack2(__uint_as_float(o[j + 6]) * inv, __uint_as_float(o[j + 7]) * inv, bf16));
                     }
-                } else if (store) {
-                    float4 *dst = reinterpret_cast<float4 *>(kp.ws_o + ((int64_t)w * kp.q_n + h) * 512 + dcol + c * 32);
+                    __syncwarp();
 #pragma unroll
-                    for (int q4 = 0; q4 < 8; ++q4)
-                        dst[q4] = make_float4(__uint_as_float(o[4 * q4]) * inv, __uint_as_float(o[4 * q4 + 1]) * inv,
-                                              __uint_as_float(o[4 * q4 + 2]) * inv, __uint_as_float(o[4 * q4 + 3]) * inv);
+                    for (int k = 0; k < 4; ++k) {
+                        const int lr = rd_row(k), hh = row_head(lr);
+                        const uint4 v = *reinterpret_cast<const uint4 *>(stage + lr * 64 + ((spiece ^ (lr & 3)) << 4));
+                        if (hh < nh)
+                            *reinterpret_cast<uint4 *>(obase + (int64_t)hh * 512 + row_dcol(lr) + c * 32 + spiece * 8) = v;
+                    }
+                }
+            } else if (ws_ok) {
+                float *wbase = kp.ws_o + ((int64_t)w * kp.q_n + h0) * 512;
+#pragma unroll 1
+                for (int c = 0; c < 16; ++c) {                   // 16 columns per chunk
+                    uint32_t o[16];
+                    __syncwarp();
+                    tmem_ld16(tmem + lane_base + TM_O + c * 16, o);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        *reinterpret_cast<float4 *>(stage + lane * 64 + ((q ^ (lane & 3)) << 4)) = make_float4(
+                            __uint_as_float(o[4 * q]) * inv, __uint_as_float(o[4 * q + 1]) * inv,
+                            __uint_as_float(o[4 * q + 2]) * inv, __uint_as_float(o[4 * q + 3]) * inv);
+                    __syncwarp();
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const int lr = rd_row(k), hh = row_head(lr);
+                        const float4 v = *reinterpret_cast<const float4 *>(stage + lr * 64 + ((spiece ^ (lr & 3)) << 4));
+                        if (hh < nh)
+                            *reinterpret_cast<float4 *>(wbase + (int64_t)hh * 512 + row_dcol(lr) + c * 16 + spiece * 4) = v;
+                    }
                 }
             }
-            if (head_row && store) {
+            __syncwarp();
+            if (head_row && h < nh && ws_ok) {
                 const float lse = ll > 0.f ? (mm + log2f(ll)) * 0.6931471805599453f : -INFINITY;
+                const int64_t row = (int64_t)s.t * kp.q_n + h0 + h;
                 if (final_split) {
                     if (kp.lse) kp.lse[row] = lse;
                 } else {
-                    kp.ws_lse[(int64_t)w * kp.q_n + h] = lse;
+                    kp.ws_lse[(int64_t)w * kp.q_n + h0 + h] = lse;
                 }
             }
             tc_fence_before();
@@ -486,8 +566,7 @@ cudaError_t launch_attn_tc(const KParams &kp, cudaStream_t st)
     cudaError_t e = cudaFuncSetAttribute(sfm_attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kSmemBytes);
     if (e != cudaSuccess) return e;
-    sfm_attn_tc_kernel<<<kp.G, kThreads, kSmemBytes, st>>>(kp);
-    return cudaGetLastError();
+    return launch_dependent(sfm_attn_tc_kernel, dim3(kp.G), dim3(kThreads), kSmemBytes, st, kp);
 }
 
 }  // namespace sfm

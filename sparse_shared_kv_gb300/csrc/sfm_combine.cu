@@ -41,6 +41,7 @@ __global__ void __launch_bounds__(kThreads) sfm_combine_kernel(KParams kp)
 {
     const int t = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int h = blockIdx.y * kHeadsPerBlock + warp;
+    grid_dependency_wait();      // partial results come from the attention launch before this one
     const bool ok = meta_ok(kp);
     if (t == 0 && blockIdx.y == 0 && threadIdx.x == 0) {
         if (!ok) set_status(kp, SFM_STATUS_METADATA_MISMATCH | kp.meta[H_FLAGS]);
@@ -128,8 +129,7 @@ cudaError_t launch_combine(const KParams &kp, cudaStream_t st)
 {
     if (kp.T == 0) return cudaSuccess;
     dim3 grid(kp.T, (kp.q_n + kHeadsPerBlock - 1) / kHeadsPerBlock);
-    sfm_combine_kernel<<<grid, kThreads, 0, st>>>(kp);
-    return cudaGetLastError();
+    return launch_dependent(sfm_combine_kernel, grid, dim3(kThreads), (size_t)0, st, kp);
 }
 
 cudaError_t launch_debug(const KParams &kp, cudaStream_t st)

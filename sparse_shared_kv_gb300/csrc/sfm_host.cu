@@ -72,10 +72,11 @@ int validate_params(const sfm_params *pp)
     return SFM_OK;
 }
 
-// The tensor-core kernel covers plain bf16 / fp16 rows with up to 64 heads.
+// The tensor-core kernel covers plain bf16 / fp16 rows; more than 64 heads run
+// as two work units (head groups) per split.
 bool tc_fits(const sfm_params &p)
 {
-    return p.kv_format == SFM_KV_PLAIN && p.num_heads_q <= 64;
+    return p.kv_format == SFM_KV_PLAIN && p.num_heads_q <= 128;
 }
 
 // Required length tensors (both calls): 参数组约束 / Paged Attention参数组.
@@ -211,6 +212,7 @@ void fill_common(KParams &kp, const sfm_params &p, const Plan &pl)
     kp.split_rows = pl.split_rows;
     kp.path = pl.path;
     kp.fingerprint = (int32_t)fingerprint(p, pl);
+    kp.head_groups = pl.path == PATH_TC ? (p.num_heads_q + 63) / 64 : 1;
     kp.wcap = pl.T * pl.max_splits_per_token;
 }
 

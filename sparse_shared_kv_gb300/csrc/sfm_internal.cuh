@@ -67,6 +67,7 @@ struct KParams {
     float scale_log2;                       // softmax_scale * log2(e)
     // plan
     int32_t G, split_rows, fingerprint, path;
+    int32_t head_groups;                    // work units per split (groups of 64 heads, tensor-core path)
     int64_t ws_capacity_splits;
     int64_t wcap;                           // capacity of the split -> row map
     // tensors
@@ -261,6 +262,35 @@ __device__ __forceinline__ int split_owner(const int32_t *sp, int T, int w)
         if (sp[mid] <= w) lo = mid; else hi = mid - 1;
     }
     return lo;
+}
+
+// ----------------------------------------------------------------------------
+// programmatic dependent launch: a kernel launched with
+// launch_dependent() may start while its predecessor in the stream is still
+// running; it must call grid_dependency_wait() before it reads anything the
+// predecessor writes.  grid_launch_dependents() lets the next kernel start.
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... Args>
+inline cudaError_t launch_dependent(void (*kernel)(Args...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                                    Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
 // ----------------------------------------------------------------------------

@@ -8,9 +8,15 @@
 //     ceil(n_t / split_rows) splits -- a function of the row's own count and
 //     the params only, so a row's arithmetic never depends on the rest of the
 //     batch (the 确定性计算 section makes batch invariance the default);
-//   * per worker (persistent CTA or CTA pair): a contiguous range of splits
-//     chosen so that every worker gets about the same modelled cost
-//     (attended rows + a fixed per-split overhead).
+//   * per query row: the lengths / window / position counts the attention
+//     kernels need (so they skip the length walk), and the split -> row map;
+//   * per worker (persistent CTA): a contiguous range of splits chosen so that
+//     every worker gets about the same modelled cost (attended rows plus a
+//     fixed per-split latency cost).
+// Each row's lengths are read once (phase 1, one row per thread); the prefix
+// sums (phase 2, contiguous runs per thread) recompute the counts from the
+// per-row records, and the worker searches (phase 3) run on shared-memory
+// copies of the prefixes when the rows fit.
 #include "sfm_internal.cuh"
 
 namespace sfm {
@@ -18,35 +24,72 @@ namespace sfm {
 namespace {
 
 constexpr int kPlanThreads = 1024;
+constexpr int kSmemRows = 2048;          // rows whose prefixes are kept in shared memory
+
+// Exclusive prefix sums of two values per thread over the block: a shuffle
+// scan inside each warp, then one warp scans the 32 warp totals.
+__device__ __forceinline__ int64_t shfl_up64(int64_t v, int d)
+{
+    return __shfl_up_sync(0xffffffffu, v, d);
+}
 
 __device__ __forceinline__ void block_exclusive_scan2(int64_t &a, int64_t &b, int64_t *sa, int64_t *sb)
 {
-    const int tid = threadIdx.x;
-    sa[tid] = a;
-    sb[tid] = b;
-    __syncthreads();
-    for (int off = 1; off < kPlanThreads; off <<= 1) {
-        int64_t va = 0, vb = 0;
-        if (tid >= off) {
-            va = sa[tid - off];
-            vb = sb[tid - off];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    int64_t ia = a, ib = b;                 // inclusive within the warp
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const int64_t ua = shfl_up64(ia, d), ub = shfl_up64(ib, d);
+        if (lane >= d) {
+            ia += ua;
+            ib += ub;
         }
-        __syncthreads();
-        sa[tid] += va;
-        sb[tid] += vb;
-        __syncthreads();
     }
-    const int64_t ia = sa[tid], ib = sb[tid];
-    a = ia - a;    // exclusive
-    b = ib - b;
+    if (lane == 31) {
+        sa[warp] = ia;
+        sb[warp] = ib;
+    }
     __syncthreads();
+    if (warp == 0) {
+        int64_t wa = lane < kPlanThreads / 32 ? sa[lane] : 0, wb = lane < kPlanThreads / 32 ? sb[lane] : 0;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int64_t ua = shfl_up64(wa, d), ub = shfl_up64(wb, d);
+            if (lane >= d) {
+                wa += ua;
+                wb += ub;
+            }
+        }
+        if (lane < kPlanThreads / 32) {
+            sa[lane] = wa;          // inclusive warp-total prefix
+            sb[lane] = wb;
+        }
+    }
+    __syncthreads();
+    const int64_t base_a = warp > 0 ? sa[warp - 1] : 0, base_b = warp > 0 ? sb[warp - 1] : 0;
+    a = base_a + ia - a;            // exclusive
+    b = base_b + ib - b;
+    __syncthreads();
+}
+
+__device__ __forceinline__ int64_t row_positions(const int32_t *rec, int t)
+{
+    const int32_t *r = rec + (int64_t)kRecWords * t;
+    return (int64_t)r[6] + r[7];
 }
 
 __global__ void __launch_bounds__(kPlanThreads) sfm_plan_kernel(KParams kp)
 {
     __shared__ int64_t s_a[kPlanThreads];
     __shared__ int64_t s_b[kPlanThreads];
+    __shared__ int32_t s_n[kSmemRows];
+    __shared__ int32_t s_sp[kSmemRows + 1];
+    __shared__ int32_t s_cp[kSmemRows + 1];
     __shared__ int s_overflow;
+
+    // the attention kernel may start its set-up now; it waits for this grid
+    // to finish before it reads the plan
+    grid_launch_dependents();
 
     int32_t *meta = kp.meta_w;
     const int T = kp.T, G = kp.G, S = kp.split_rows;
@@ -55,6 +98,7 @@ __global__ void __launch_bounds__(kPlanThreads) sfm_plan_kernel(KParams kp)
     int32_t *cp = meta + meta_cost_off(G, T);
     int32_t *rec = meta + meta_rec_off(G, T);
     int32_t *own = meta + meta_own_off(G, T);
+    const bool in_smem = T <= kSmemRows;
     const int tid = threadIdx.x;
     if (tid == 0) {
         s_overflow = 0;
@@ -63,27 +107,9 @@ __global__ void __launch_bounds__(kPlanThreads) sfm_plan_kernel(KParams kp)
     __syncthreads();
     kp.status = meta + H_LENFLAGS;
 
-    // 1. per-row split count and cost; each thread owns a contiguous run of rows
-    const int per = (T + kPlanThreads - 1) / kPlanThreads;
-    const int beg = min(T, tid * per), end = min(T, beg + per);
-    int64_t sum_s = 0, sum_c = 0;
-    for (int t = beg; t < end; ++t) {
+    // 1. every row once: its record (and its position count)
+    for (int t = tid; t < T; t += kPlanThreads) {
         const Tok k = token_info(kp, t);
-        const int64_t n = (int64_t)k.n_ori + k.n_cmp;
-        const int64_t ns = n > 0 ? (n + S - 1) / S : 0;
-        sum_s += ns;
-        sum_c += n + ns * kSplitOverheadRows;
-    }
-    // 2. exclusive scan of the per-thread sums, then the per-row prefixes
-    int64_t ex_s = sum_s, ex_c = sum_c;
-    block_exclusive_scan2(ex_s, ex_c, s_a, s_b);
-    for (int t = beg; t < end; ++t) {
-        const Tok k = token_info(kp, t);
-        const int64_t n = (int64_t)k.n_ori + k.n_cmp;
-        const int64_t ns = n > 0 ? (n + S - 1) / S : 0;
-        if (ex_s > INT32_MAX || ex_c > INT32_MAX || ex_s + ns > kp.wcap) s_overflow = 1;
-        sp[t] = (int32_t)ex_s;
-        cp[t] = (int32_t)ex_c;
         int32_t *r = rec + (int64_t)kRecWords * t;
         r[0] = k.b;
         r[1] = k.kv_len;
@@ -93,46 +119,81 @@ __global__ void __launch_bounds__(kPlanThreads) sfm_plan_kernel(KParams kp)
         r[5] = k.hi;
         r[6] = k.n_ori;
         r[7] = k.n_cmp;
+        if (in_smem) s_n[t] = k.n_ori + k.n_cmp;
+    }
+    __syncthreads();
+    // 2. split / cost prefixes: each thread scans a contiguous run of rows
+    const int per = (T + kPlanThreads - 1) / kPlanThreads;
+    const int beg = min(T, tid * per), end = min(T, beg + per);
+    auto count = [&](int t) -> int64_t { return in_smem ? (int64_t)s_n[t] : row_positions(rec, t); };
+    int64_t sum_s = 0, sum_c = 0;
+    for (int t = beg; t < end; ++t) {
+        const int64_t n = count(t), ns = n > 0 ? (n + S - 1) / S : 0;
+        sum_s += ns;
+        sum_c += n + ns * kSplitOverheadRows;
+    }
+    int64_t ex_s = sum_s, ex_c = sum_c;
+    block_exclusive_scan2(ex_s, ex_c, s_a, s_b);
+    for (int t = beg; t < end; ++t) {
+        const int64_t n = count(t), ns = n > 0 ? (n + S - 1) / S : 0;
+        if (ex_s > INT32_MAX || ex_c > INT32_MAX || ex_s + ns > kp.wcap) s_overflow = 1;
+        sp[t] = (int32_t)ex_s;
+        cp[t] = (int32_t)ex_c;
+        if (in_smem) {
+            s_sp[t] = (int32_t)ex_s;
+            s_cp[t] = (int32_t)ex_c;
+        }
         for (int64_t j = 0; j < ns && ex_s + j < kp.wcap; ++j) own[ex_s + j] = t;
         ex_s += ns;
         ex_c += n + ns * kSplitOverheadRows;
     }
-    if (tid == kPlanThreads - 1) {
+    if ((beg < end && end == T) || (T == 0 && tid == 0)) {   // the run that ends the rows writes the totals
         if (ex_s > INT32_MAX || ex_c > INT32_MAX) s_overflow = 1;
         sp[T] = (int32_t)ex_s;
         cp[T] = (int32_t)ex_c;
+        if (in_smem) {
+            s_sp[T] = (int32_t)ex_s;
+            s_cp[T] = (int32_t)ex_c;
+        }
     }
     __syncthreads();
 
-    // 3. worker ranges: worker c starts at the first split whose cumulative
-    //    cost reaches c / G of the total
-    const int32_t W = sp[T];
-    const int64_t total = cp[T];
+    // 3. worker ranges over work units: a unit is one split for one group of
+    //    heads (head_groups units per split, consecutive); worker c starts at
+    //    the first unit whose cumulative cost reaches c / G of the total
+    const int32_t *xsp = in_smem ? s_sp : sp;
+    const int32_t *xcp = in_smem ? s_cp : cp;
+    const int64_t HG = kp.head_groups;
+    const int32_t W = xsp[T];
+    const int64_t units = (int64_t)W * HG;
+    if (units > INT32_MAX && tid == 0) s_overflow = 1;
+    const int64_t total = (int64_t)xcp[T] * HG;
     for (int c = tid; c <= G; c += kPlanThreads) {
-        int32_t w;
+        int64_t u;
         if (c == 0) {
-            w = 0;
+            u = 0;
         } else if (c == G) {
-            w = W;
+            u = units;
         } else {
             const int64_t target = total * c / G;
-            int lo = 0, hi = T;     // last row t with cp[t] <= target
+            int lo = 0, hi = T;     // last row t whose cumulative cost <= target
             while (lo < hi) {
                 int mid = (lo + hi + 1) >> 1;
-                if (cp[mid] <= target) lo = mid; else hi = mid - 1;
+                if ((int64_t)xcp[mid] * HG <= target) lo = mid; else hi = mid - 1;
             }
             if (lo >= T) {
-                w = W;
+                u = units;
             } else {
-                const int64_t ns = sp[lo + 1] - sp[lo];
-                const int64_t within = target - cp[lo];
-                int64_t s = (within + S + kSplitOverheadRows - 1) / (S + kSplitOverheadRows);
-                if (s > ns) s = ns;
-                w = sp[lo] + (int32_t)s;
+                const int64_t nu = (int64_t)(xsp[lo + 1] - xsp[lo]) * HG;
+                const int64_t within = target - (int64_t)xcp[lo] * HG;
+                int64_t k = (within + S + kSplitOverheadRows - 1) / (S + kSplitOverheadRows);
+                if (k > nu) k = nu;
+                u = (int64_t)xsp[lo] * HG + k;
             }
         }
-        ws[c] = w;
+        ws[c] = (int32_t)(u < INT32_MAX ? u : INT32_MAX);
     }
+    __syncthreads();
     if (tid == 0) {
         meta[H_MAGIC] = kMetaMagic;
         meta[H_FPRINT] = kp.fingerprint;

@@ -272,7 +272,7 @@ def test_kernel_paths_tiny(name, kw, hint):
 
 
 @pytest.mark.parametrize("hint", [1, 2], ids=["cuda_core", "tensor_core"])
-@pytest.mark.parametrize("q_n", [1, 8, 16, 32, 40, 64])
+@pytest.mark.parametrize("q_n", [1, 8, 16, 32, 40, 64, 65, 96, 128])
 def test_kernel_paths_heads(q_n, hint):
     prob = S.build(f"heads{q_n}", seed=100 + q_n, device="cuda", q_n=q_n, q_lens=[1, 1, 1, 1],
                    kv_lens=[700, 1500, 300, 20000], layout_q="BSND", layout_kv="PAGED", mode="csa", cmp_ratio=4,
@@ -293,7 +293,9 @@ def test_kernel_paths_prefill_fp16(hint):
 
 
 def test_tensor_core_hint_rejects_unsupported():
-    prob = S.build("q128", seed=1, device="cuda", q_n=128, q_lens=[1], kv_lens=[300], layout_q="BSND",
-                   layout_kv="BSND", mode="swa")
+    # quantized packed rows have no tensor-core path; asking for one is an error
+    prob = S.build("packed_tc", seed=1, device="cuda", q_n=16, q_lens=[1], kv_lens=[300], layout_q="BSND",
+                   layout_kv="PAGED", mode="ori_sparse", ori_topk=64, ori_mask_mode=3, cmp_mask_mode=0,
+                   kv_format="int8_packed", rope_head_dim=64, ori_block_size=64)
     with pytest.raises(sfm.SfmError):
         sfm.sfm_metadata_size(_sfm.params_of(prob, kernel_hint=2))
