@@ -149,8 +149,9 @@ __global__ void __launch_bounds__(kThreads) sfm_attn_simt_kernel(KParams kp)
         const int sidx = w - sp[t];
         const Tok k = token_info(kp, t);
         const int n = k.n_ori + k.n_cmp;
-        const int pos0 = sidx * SR;
-        const int pos1 = min(n, pos0 + SR);
+        const int size = split_size(n, SR);
+        const int pos0 = sidx * size;
+        const int pos1 = min(n, pos0 + size);
         const bool final_split = nsplit == 1;
         if (!final_split && w >= kp.ws_capacity_splits) {
             set_status(kp, SFM_STATUS_WORKSPACE_OVERFLOW);
@@ -256,9 +257,9 @@ __global__ void __launch_bounds__(kThreads) sfm_attn_simt_kernel(KParams kp)
                 if (tid == 0 && kp.lse) kp.lse[row] = l > 0.f ? m + logf(l) : -INFINITY;
             } else {
                 const float inv = l > 0.f ? 1.f / l : 0.f;
-                float *o = kp.ws_o + ((int64_t)w * kp.q_n + hh) * 512;
-                o[tid] = acc[h][0] * inv;
-                o[tid + 256] = acc[h][1] * inv;
+                uint16_t *o = kp.ws_o + ((int64_t)w * kp.q_n + hh) * 512;
+                o[tid] = float_to_half(acc[h][0] * inv, SFM_DTYPE_BF16);
+                o[tid + 256] = float_to_half(acc[h][1] * inv, SFM_DTYPE_BF16);
                 if (tid == 0) kp.ws_lse[(int64_t)w * kp.q_n + hh] = l > 0.f ? m + logf(l) : -INFINITY;
             }
         }

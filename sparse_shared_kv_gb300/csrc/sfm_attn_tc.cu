@@ -1,35 +1,59 @@
 // sfm_attn_tc.cu -- tensor-core (tcgen05 / TMEM) split-KV attention for
 // plain bf16 / fp16 KV rows.
 //
-// One persistent CTA per SM walks the work units the planner gave its worker;
-// a unit is one split for one group of up to 64 query heads (128 heads make
-// two units per split, whose second pass over the split's rows hits L2).
-// Per 64-row KV tile of a split:
-//   producer warps 0-1   resolve the attended rows (window / compressed /
-//                        indices through the block tables) and stream each
-//                        1 KB row with cp.async into a 128-byte-swizzled
-//                        shared-memory stage (two stages);
-//   MMA warp 2           S = Q.K~^T            (M=128, N=64,  K=512)   -> TMEM
-//                        O += P.V~             (M=128, N=256, K=2x64)  -> TMEM
-//                        both reading the SAME staged tile (K-major for S,
-//                        MN-major for P.V);
-//   softmax warps 4-7    one thread per score row: scale, mask, running max
-//                        with lazy rescaling, exp2, row sum, P (bf16/fp16)
-//                        into shared memory; the epilogue normalises O and
-//                        writes the output (single split) or the split's
-//                        partial O and LSE for the combine kernel.
+// One persistent CTA per SM walks the work units the planner gave its worker.
+// A unit is one split of one query row for one group of up to 64 heads; the
+// units of a row are ordered group-major, so consecutive units of a worker
+// usually share their Q rows and Q is only reloaded when the (row, group)
+// changes.  Per 32-row KV tile of a unit:
+//   resolver warp 9      resolves the attended rows (window / compressed /
+//                        indices through the block tables) up to 16 tiles
+//                        ahead, four tiles per batch so that a batch costs
+//                        two dependent memory round trips, into a ring of
+//                        row numbers in shared memory;
+//   producer warps 0-3   stream each tile's 32 rows (1 KB each, 8 rows per
+//                        warp) with cp.async into the 128-byte-swizzled
+//                        operand layout (four stages) and, when the (row,
+//                        head group) changes, the unit's 64 Q rows (16 per
+//                        warp).  Four copy warps keep more requests in
+//                        flight per SM than two (about 38 vs 33 GB/s per SM
+//                        with all SMs loading).  16-byte cp.async
+//                        gathers sustain about 5 TB/s of random 1 KB rows on
+//                        this part; TMA row gathers (tile::gather4) reach
+//                        about 1.8 TB/s, one-row TMA boxes about 0.7 TB/s;
+//   MMA warps 8, 10      S = Q.K~^T            (M=128, N=32,  K=512)   -> TMEM
+//                        as two independent accumulation chains (K halves);
+//   MMA in warp 6        O += P.V~             (M=128, N=256, K=2x32)  -> TMEM
+//                        both products read the SAME staged tile (K-major
+//                        for S, MN-major for P.V); four S buffers, two P
+//                        buffers.  A chain of small dependent MMAs from one
+//                        thread is bound by per-instruction latency, not by
+//                        the math, so S is split in two chains on two warps
+//                        and P.V has its own issuing warp;
+//   softmax warps 4-7    warps 4-5: one thread per head row -- scale, mask,
+//                        running max with lazy rescaling, exp2, row sum, P
+//                        (bf16/fp16) into shared memory; warps 6-7 rescale the
+//                        upper half of O.  The epilogue pulls O out of TMEM
+//                        into registers (releasing TMEM for the next unit's
+//                        first P.V) and writes the output (single split) or
+//                        the split's bf16 partial O and fp32 LSE for the
+//                        combine kernel.
 //
 // M=128 rows with at most 64 heads: the upper 64 rows of the Q operand alias
 // the next column block (their scores are never read), and O uses a
 // block-diagonal P so that TMEM rows 0-63 accumulate O[:, 0:256] and rows
 // 64-127 accumulate O[:, 256:512] in 256 columns: A = [P;0] with V[:, :256]
-// for the first 64 reduction steps, A = [0;P] with V[:, 256:] for the next.
+// for the first two reduction steps, A = [0;P] with V[:, 256:] for the next.
 //
 // Softmax follows the pages' definition (S = Q.K~^T * softmax_scale, softmax
 // over the attended rows, LSE = max S + log sum exp(S - max S)); scores are
 // kept in the log2 domain (x = S * log2 e) and the running max is only moved
 // when a row's max grows by more than 8 (a factor 256), which leaves O / l
 // unchanged mathematically and keeps fp32 far from overflow.
+//
+// Every wait is bounded (2 s); a timeout raises the CTA's abort flag, every
+// role leaves its loop at its next wait, in-flight copies and MMAs are
+// drained, TMEM is freed and SFM_STATUS_TIMEOUT is reported.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <math.h>
@@ -43,61 +67,97 @@ namespace {
 
 using namespace tc;
 
-constexpr int NT = 64;                       // KV rows per tile
-constexpr int kThreads = 256;
+constexpr int NT = 32;                       // KV rows per tile
+constexpr int kStages = 4;                   // KV stages == S buffers
+constexpr int kThreads = 384;               // 12 warps: three warpgroups
+constexpr int kProducers = 4;               // KV copy warps
 constexpr uint32_t Q_OFF = 0;                // 8 blocks x 64 rows x 128 B
 constexpr uint32_t P_OFF = 65536;            // 192 rows x 128 B: [0..63] zero, [64..127] P, [128..191] zero
-constexpr uint32_t KV_OFF = 90112;           // 2 stages x 64 KB
-constexpr uint32_t KV_STAGE = 65536;
-constexpr uint32_t MISC_OFF = KV_OFF + 2 * KV_STAGE;   // 221184
-constexpr uint32_t kSmemBytes = MISC_OFF + 1536 + 1024;   // misc block (1280 B used) + alignment slack
+constexpr uint32_t KV_OFF = 90112;           // 4 stages x 32 KB
+constexpr uint32_t KV_BLOCK = NT * 128;      // one 64-column block of a stage
+constexpr uint32_t KV_STAGE = 8 * KV_BLOCK;
+constexpr uint32_t MISC_OFF = KV_OFF + kStages * KV_STAGE;   // 221184
+constexpr uint32_t MISC_BYTES = 4608;
+constexpr uint32_t EPI_OFF = MISC_OFF + MISC_BYTES;          // epilogue staging, 1 KB per softmax warp
+constexpr uint32_t kSmemBytes = EPI_OFF + 4 * 1024 + 1024;   // + alignment slack
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t TM_O = 0;                 // O: columns [0, 256)
-constexpr uint32_t TM_S = 256;               // S buffers: [256, 320), [320, 384)
+constexpr uint32_t TM_S = 256;               // S buffer s: [256 + 64 s, 320 + 64 s), two 32-column halves
 constexpr float kRescaleThreshold = 8.0f;    // log2 units
+constexpr int kRing = 16;                    // resolved tiles in flight
+constexpr int kResolveBatch = 4;             // tiles per resolver batch
+
+static_assert(kSmemBytes <= 232448, "shared memory budget");
+static_assert(P_OFF == Q_OFF + 8 * 8192, "the last Q block's alias rows must be P's leading zero rows");
 
 // barrier slots (8 bytes each) at MISC_OFF
 enum Bar {
-    B_KV_FULL = 0, B_KV_EMPTY = 2, B_S_FULL = 4, B_S_FREE = 6, B_P_FULL = 8, B_O_DONE = 9, B_Q_FULL = 10,
-    B_Q_EMPTY = 11, B_O_FREE = 12, B_TEARDOWN = 13, B_ALPHA = 14, B_STATS = 16, kNumBars = 17
+    B_KV_FULL = 0,     // [4] 128 copy-completion arrivals + the row-mask word
+    B_KV_EMPTY = 4,    // [4] P.V of the tile done
+    B_S_FULL = 8,      // [4] both halves of S of the tile in TMEM
+    B_S_FREE = 12,     // [4] both head warps read S
+    B_P_FULL = 16,     // [2] P written and O rescaled by all four softmax warps
+    B_O_DONE = 18,     // [2] P.V of tiles with that parity done
+    B_Q_FULL = 20,     // 128 copy-completion arrivals
+    B_Q_EMPTY = 21,    // both S issuers done with Q
+    B_ALPHA = 22,      // [4] per-tile rescale factors published
+    B_STATS = 26,      // final (max, sum) of the unit published
+    B_TEARDOWN = 27,
+    B_ROW_FULL = 28,   // [16] resolved rows of a tile in the ring
+    B_ROW_EMPTY = 44,  // [16] the four producer warps took them
+    B_TEARDOWN_PV = 60,
+    B_TEARDOWN_S2 = 61,
+    kNumBars = 62
 };
-constexpr uint32_t TMEM_SLOT_OFF = MISC_OFF + 128;
-constexpr uint32_t ABORT_OFF = MISC_OFF + 132;
-constexpr uint32_t VALID_OFF = MISC_OFF + 144;   // [2 stages][2 words]
-constexpr uint32_t ALPHA_OFF = MISC_OFF + 256;   // [2][64] floats
-constexpr uint32_t STATS_OFF = MISC_OFF + 768;   // [64][2] floats
+constexpr uint32_t TMEM_SLOT_OFF = MISC_OFF + 512;
+constexpr uint32_t ABORT_OFF = MISC_OFF + 516;
+constexpr uint32_t VALID_OFF = MISC_OFF + 528;   // [4] row-valid words
+constexpr uint32_t ALPHA_OFF = MISC_OFF + 1024;  // [4][64] floats
+constexpr uint32_t STATS_OFF = MISC_OFF + 2048;  // [64][2] floats
+constexpr uint32_t RING_OFF = MISC_OFF + 2560;   // [16][32] int32 row entries
+static_assert(kNumBars * 8 <= 512, "barrier area");
+static_assert(RING_OFF + kRing * NT * 4 <= MISC_OFF + MISC_BYTES, "misc area");
 
-struct SplitInfo {
-    int t, sidx, nsplit, pos0, pos1, ntiles;
+struct Unit {
+    int t, w, h0, nh, nsplit, pos0, pos1, ntiles, key;
     Tok k;
 };
 
-// The split's row and that row's lengths / window / position counts come
-// from the plan (two dependent loads instead of a search and a length walk).
-__device__ __forceinline__ SplitInfo split_info(const KParams &kp, const int32_t *sp, int w)
+// Unit u of the plan: its query row, split, head group and row range.  Two
+// dependent loads (split -> row -> row record) instead of a search and a
+// length walk.
+__device__ __forceinline__ Unit unit_info(const KParams &kp, const int32_t *sp, int u)
 {
-    SplitInfo s;
-    s.t = kp.meta[meta_own_off(kp.G, kp.T) + w];
+    Unit s;
+    const int HG = kp.head_groups;
+    s.t = __ldg(kp.meta + meta_own_off(kp.G, kp.T) + u / HG);
     const int32_t *rec = kp.meta + meta_rec_off(kp.G, kp.T) + (int64_t)kRecWords * s.t;
-    const int s_beg = sp[s.t], s_end = sp[s.t + 1];
+    const int s_beg = __ldg(sp + s.t), s_end = __ldg(sp + s.t + 1);
     s.nsplit = s_end - s_beg;
-    s.sidx = w - s_beg;
+    const int local = u - s_beg * HG;
+    const int hg = s.nsplit > 0 ? local / s.nsplit : 0;
+    const int sidx = local - hg * s.nsplit;
+    s.w = s_beg + sidx;
+    s.h0 = hg * 64;
+    s.nh = min(64, kp.q_n - s.h0);
+    s.key = s.t * HG + hg;
     Tok &k = s.k;
-    k.b = rec[0];
-    k.kv_len = rec[1];
-    k.cmp_len = rec[2];
-    k.p_cmp = rec[3];
-    k.lo = rec[4];
-    k.hi = rec[5];
-    k.n_ori = rec[6];
-    k.n_cmp = rec[7];
+    k.b = __ldg(rec + 0);
+    k.kv_len = __ldg(rec + 1);
+    k.cmp_len = __ldg(rec + 2);
+    k.p_cmp = __ldg(rec + 3);
+    k.lo = __ldg(rec + 4);
+    k.hi = __ldg(rec + 5);
+    k.n_ori = __ldg(rec + 6);
+    k.n_cmp = __ldg(rec + 7);
     k.i = 0;
     k.q_len = 0;
     k.p = 0;
     k.valid = 1;
     const int n = k.n_ori + k.n_cmp;
-    s.pos0 = s.sidx * kp.split_rows;
-    s.pos1 = min(n, s.pos0 + kp.split_rows);
+    const int size = split_size(n, kp.split_rows);
+    s.pos0 = sidx * size;
+    s.pos1 = min(n, s.pos0 + size);
     const int rows = s.pos1 > s.pos0 ? s.pos1 - s.pos0 : 0;
     s.ntiles = rows > 0 ? (rows + NT - 1) / NT : 1;   // an empty split still runs one masked tile
     return s;
@@ -113,7 +173,58 @@ __device__ __forceinline__ uint32_t pack2(float a, float b, bool bf16)
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
-__global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(KParams kp)
+// Row entries of this lane's row in tiles i0 .. i0+K-1 of the unit: -1 for a
+// skipped or masked position, else the pool row with bit 31 set for the
+// compressed pool.  Same rules and status bits as resolve_row(); every index
+// load of the batch is issued before any block-table load.
+template <int K>
+__device__ __forceinline__ void resolve_tiles(const KParams &kp, const Unit &s, int i0, int lane, int32_t (&ent)[K])
+{
+    const Tok &k = s.k;
+    int e[K];
+    bool in[K], cmp[K];
+#pragma unroll
+    for (int j = 0; j < K; ++j) {
+        const int pos = s.pos0 + (i0 + j) * NT + lane;
+        in[j] = pos < s.pos1;
+        cmp[j] = pos >= k.n_ori;
+        const int jj = pos - k.n_ori;
+        e[j] = cmp[j] ? jj : k.lo + pos;
+        if (in[j]) {
+            if (!cmp[j] && kp.ori_topk > 0) e[j] = __ldg(kp.ori_idx + (int64_t)s.t * kp.ori_topk + pos);
+            else if (cmp[j] && kp.cmp_topk > 0) e[j] = __ldg(kp.cmp_idx + (int64_t)s.t * kp.cmp_topk + jj);
+        }
+    }
+    int err = 0;
+    int64_t row[K];
+#pragma unroll
+    for (int j = 0; j < K; ++j) {
+        bool ok = in[j];
+        if (ok && !cmp[j] && kp.ori_topk > 0) {
+            if (e[j] >= k.kv_len) err |= SFM_STATUS_BAD_INDEX;
+            ok = e[j] >= 0 && e[j] < k.kv_len && e[j] >= k.lo && e[j] <= k.hi;
+        } else if (ok && cmp[j] && kp.cmp_topk > 0) {
+            if (e[j] >= k.cmp_len) err |= SFM_STATUS_BAD_INDEX;
+            ok = e[j] >= 0 && e[j] < k.cmp_len &&
+                 (kp.cmp_mask_mode != 3 || (int64_t)(e[j] + 1) * kp.cmp_ratio <= (int64_t)k.p_cmp + 1);
+        }
+        in[j] = ok;
+        row[j] = ok ? phys_row(kp, cmp[j] ? 1 : 0, k.b, e[j]) : 0;
+    }
+#pragma unroll
+    for (int j = 0; j < K; ++j) {
+        int32_t v = -1;
+        if (in[j]) {
+            const int64_t nrows = cmp[j] ? kp.cmp_rows : kp.ori_rows;
+            if (row[j] < 0 || row[j] >= nrows) err |= SFM_STATUS_BAD_BLOCK;
+            else v = static_cast<int32_t>(static_cast<uint32_t>(row[j]) | (cmp[j] ? 0x80000000u : 0u));
+        }
+        ent[j] = v;
+    }
+    if (err) set_status(kp, err);
+}
+
+__global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(const KParams kp)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -133,28 +244,32 @@ __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(KParams kp)
     for (uint32_t i = tid; i < 24576u / 16u; i += kThreads)
         reinterpret_cast<uint4 *>(base + P_OFF)[i] = make_uint4(0, 0, 0, 0);
     if (tid == 0) {
-        mbar_init(bar(B_KV_FULL + 0), 66);   // 64 copy-completion arrivals + 2 row-mask words
-        mbar_init(bar(B_KV_FULL + 1), 66);
-        mbar_init(bar(B_KV_EMPTY + 0), 1);
-        mbar_init(bar(B_KV_EMPTY + 1), 1);
-        mbar_init(bar(B_S_FULL + 0), 1);
-        mbar_init(bar(B_S_FULL + 1), 1);
-        mbar_init(bar(B_S_FREE + 0), 128);
-        mbar_init(bar(B_S_FREE + 1), 128);
-        mbar_init(bar(B_P_FULL), 128);
-        mbar_init(bar(B_O_DONE), 1);
-        mbar_init(bar(B_Q_FULL), 64);
-        mbar_init(bar(B_Q_EMPTY), 1);
-        mbar_init(bar(B_O_FREE), 128);
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(bar(B_KV_FULL + s), 32 * kProducers + 1);
+            mbar_init(bar(B_KV_EMPTY + s), 1);
+            mbar_init(bar(B_S_FULL + s), 2);
+            mbar_init(bar(B_S_FREE + s), 2);
+            mbar_init(bar(B_ALPHA + s), 2);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar(B_P_FULL + b), 4);
+            mbar_init(bar(B_O_DONE + b), 1);
+        }
+        for (int r = 0; r < kRing; ++r) {
+            mbar_init(bar(B_ROW_FULL + r), 1);
+            mbar_init(bar(B_ROW_EMPTY + r), kProducers);
+        }
+        mbar_init(bar(B_Q_FULL), 32 * kProducers);
+        mbar_init(bar(B_Q_EMPTY), 2);
+        mbar_init(bar(B_STATS), 2);
         mbar_init(bar(B_TEARDOWN), 1);
-        mbar_init(bar(B_ALPHA + 0), 64);
-        mbar_init(bar(B_ALPHA + 1), 64);
-        mbar_init(bar(B_STATS), 64);
+        mbar_init(bar(B_TEARDOWN_PV), 1);
+        mbar_init(bar(B_TEARDOWN_S2), 1);
         *abort_flag = 0;
         fence_barrier_init();
     }
     fence_proxy_async_smem();
-    if (warp == 2) {
+    if (warp == 8) {
         tmem_alloc(sb + TMEM_SLOT_OFF, kTmemCols);
         tmem_relinquish();
     }
@@ -168,32 +283,64 @@ __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(KParams kp)
     const bool ok = meta_ok(kp);
     const int worker = blockIdx.x;
     const int32_t *sp = kp.meta + meta_split_off(kp.G);
-    const int w_beg = ok ? kp.meta[meta_ws_off() + worker] : 0;
-    const int w_end = ok ? kp.meta[meta_ws_off() + worker + 1] : 0;
+    const int u_beg = ok ? __ldg(kp.meta + meta_ws_off() + worker) : 0;
+    const int u_end = ok ? __ldg(kp.meta + meta_ws_off() + worker + 1) : 0;
 
-    if (warp < 2) {
-        // ======================= producer =======================
-        // Thread pt owns tile row pt (and Q head row pt).  Copies arrive on the
-        // stage barrier by themselves when they land (cp.async.mbarrier), so
-        // the producer never waits for its own loads; it only waits for a
-        // free stage.  Rows are resolved one tile ahead of the tile in flight.
-        const int pt = tid;
-        const uint8_t *zero_src = static_cast<const uint8_t *>(kp.q);
-        int g = 0, ks = 0;
+    int32_t *ring = reinterpret_cast<int32_t *>(base + RING_OFF);
+
+
+    if (warp == 9) {
+        // ======================= row resolver =======================
+        // Lane L resolves row L of every tile, kResolveBatch tiles at a time,
+        // and publishes each tile's 32 entries in ring slot (tile % kRing).
+        int g = 0;
         bool stop = false;
-        for (int u = w_beg; u < w_end && !stop; ++u) {
-            const int w = u / kp.head_groups, h0 = (u - w * kp.head_groups) * 64;
-            const int nh = min(64, kp.q_n - h0);
-            const SplitInfo s = split_info(kp, sp, w);
-            if (ks > 0 && !warp_wait(bar(B_Q_EMPTY), (ks - 1) & 1, abort_flag)) break;
-            {
-                // Q rows of this warp's 32 heads, one 1 KB row per step: lane L
-                // copies 16-byte chunks L and L + 32 (512 contiguous bytes per
-                // instruction)
-                const uint8_t *qrow = static_cast<const uint8_t *>(kp.q) + ((int64_t)s.t * kp.q_n + h0) * 1024;
-                for (int rr = 0; rr < 32; ++rr) {
-                    const int hh = warp * 32 + rr;
-                    const bool live = hh < nh;
+        Unit cur = u_beg < u_end ? unit_info(kp, sp, u_beg) : Unit{};
+        for (int u = u_beg; u < u_end && !stop; ++u) {
+            const Unit nxt = u + 1 < u_end ? unit_info(kp, sp, u + 1) : cur;   // prefetched
+            const Unit &s = cur;
+            for (int i0 = 0; i0 < s.ntiles && !stop; i0 += kResolveBatch) {
+                int32_t ent[kResolveBatch];
+                resolve_tiles<kResolveBatch>(kp, s, i0, lane, ent);
+#pragma unroll
+                for (int j = 0; j < kResolveBatch; ++j) {
+                    const int i = i0 + j;
+                    if (i >= s.ntiles) break;
+                    const int gi = g + i, slot = gi % kRing, use = gi / kRing;
+                    if (use >= 1 && !warp_wait(bar(B_ROW_EMPTY + slot), (use - 1) & 1, abort_flag)) {
+                        stop = true;
+                        break;
+                    }
+                    ring[slot * NT + lane] = ent[j];
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(B_ROW_FULL + slot));
+                }
+            }
+            g += s.ntiles;
+            cur = nxt;
+        }
+    } else if (warp < kProducers) {
+        // ======================= producers =======================
+        // The four warps share every tile: warp pw copies rows 8pw..8pw+7,
+        // one 1 KB row per step (row address broadcast from the ring entry's
+        // lane; lane L copies 16-byte chunks L and L + 32: 512 contiguous
+        // bytes per warp instruction).  Copies arrive on the stage barrier by
+        // themselves when they land.  Each warp also copies 16 of the unit's
+        // 64 Q rows when the (row, head group) changes.
+        const int pw = warp;
+        constexpr int kRowsPerWarp = NT / kProducers;
+        const uint8_t *zero_src = static_cast<const uint8_t *>(kp.q);
+        int g = 0, nq = 0, prev_key = -1;
+        bool stop = false;
+        for (int u = u_beg; u < u_end && !stop; ++u) {
+            const Unit s = unit_info(kp, sp, u);
+            if (s.key != prev_key) {
+                if (nq > 0 && !warp_wait(bar(B_Q_EMPTY), (nq - 1) & 1, abort_flag)) break;
+                const uint8_t *qrow = static_cast<const uint8_t *>(kp.q) + ((int64_t)s.t * kp.q_n + s.h0) * 1024;
+#pragma unroll 4
+                for (int rr = 0; rr < 64 / kProducers; ++rr) {
+                    const int hh = pw * (64 / kProducers) + rr;
+                    const bool live = hh < s.nh;
 #pragma unroll
                     for (int half = 0; half < 2; ++half) {
                         const int C = lane + half * 32;
@@ -202,185 +349,155 @@ __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(KParams kp)
                     }
                 }
                 cp_async_arrive_noinc(bar(B_Q_FULL));
+                ++nq;
+                prev_key = s.key;
             }
-            auto resolve = [&](int i) -> const uint8_t * {
-                const int pos = s.pos0 + i * NT + pt;
-                if (pos >= s.pos1) return nullptr;
-                int logical, src;
-                return resolve_row(kp, s.k, s.t, pos, &logical, &src);
-            };
-            const uint8_t *rp[2];
-            rp[0] = resolve(0);
-            rp[1] = s.ntiles > 1 ? resolve(1) : nullptr;      // independent chains overlap
-            for (int i = 0; i < s.ntiles; ++i, ++g) {
-                const int st = g & 1, use = g >> 1;
-                if (use >= 1 && !warp_wait(bar(B_KV_EMPTY + st), (use - 1) & 1, abort_flag)) {
-                    stop = true;
-                    break;
-                }
-                const uint8_t *row = rp[i & 1];
+            for (int i = 0; i < s.ntiles; ++i) {
+                const int gi = g + i, slot = gi % kRing, st = gi & (kStages - 1), use = gi / kStages;
+                if (!warp_wait(bar(B_ROW_FULL + slot), (gi / kRing) & 1, abort_flag)) { stop = true; break; }
+                const int32_t e = ring[slot * NT + lane];
                 __syncwarp();
+                if (lane == 0) mbar_arrive(bar(B_ROW_EMPTY + slot));
+                const uint8_t *row = nullptr;
+                if (e != -1) {
+                    const int64_t r = e & 0x7fffffff;
+                    row = e < 0 ? kp.cmp_kv + r * kp.cmp_row_stride : kp.ori_kv + r * kp.ori_row_stride;
+                }
                 const uint32_t vm = __ballot_sync(0xffffffffu, row != nullptr);
+                if (use >= 1 && !warp_wait(bar(B_KV_EMPTY + st), (use - 1) & 1, abort_flag)) { stop = true; break; }
                 const uint32_t stage = sb + KV_OFF + st * KV_STAGE;
-                // this warp's 32 tile rows, one row per step (pointer broadcast
-                // from the lane that resolved it): 512 contiguous bytes per
-                // warp instruction
                 const unsigned long long my_row = reinterpret_cast<unsigned long long>(row);
-                for (int rr = 0; rr < 32; ++rr) {
+#pragma unroll
+                for (int k = 0; k < kRowsPerWarp; ++k) {
+                    const int rr = pw * kRowsPerWarp + k;
                     const uint8_t *src = reinterpret_cast<const uint8_t *>(__shfl_sync(0xffffffffu, my_row, rr));
-                    const int tr = warp * 32 + rr;
 #pragma unroll
                     for (int half = 0; half < 2; ++half) {
                         const int C = lane + half * 32;
-                        const uint32_t dst = stage + (C >> 3) * 8192u + sw128(tr, C & 7);
+                        const uint32_t dst = stage + (C >> 3) * KV_BLOCK + sw128(rr, C & 7);
                         cp_async16(dst, src ? src + C * 16 : zero_src, src ? 16u : 0u);
                     }
                 }
                 cp_async_arrive_noinc(bar(B_KV_FULL + st));
-                if (lane == 0) {
-                    valid_s[st * 2 + warp] = vm;          // this warp's 32 row-valid bits
-                    mbar_arrive(bar(B_KV_FULL + st));     // release: the word is visible with the phase
+                if (pw == 0 && lane == 0) {
+                    valid_s[st] = vm;                        // the tile's row-valid bits
+                    mbar_arrive(bar(B_KV_FULL + st));        // release: the word is visible with the phase
                 }
-                // the next tile was resolved earlier; resolve the one after it now,
-                // behind the copies in flight
-                if (i >= 1 && i + 1 < s.ntiles) rp[(i + 1) & 1] = resolve(i + 1);
             }
-            ++ks;
+            g += s.ntiles;
         }
         cp_async_wait<0>();
-    } else if (warp == 2) {
-        // ======================= MMA issuer =======================
-        // One thread polls both inputs and issues whichever product is ready:
-        // S(i) needs tile i staged and its S buffer free; P.V(i) needs P(i)
-        // (and, for a split's first tile, the previous epilogue done with O).
+    } else if (warp == 8 || warp == 10) {
+        // ======================= S issuers =======================
+        // S(i) needs tile i staged and its S buffer free.  Its 32 reduction
+        // steps run as two independent accumulation chains issued by two
+        // warps: warp 8 over dimensions 0..255, warp 10 over 256..511, into
+        // adjacent 32-column halves of the S buffer; the softmax adds them.
+        // P.V is issued by warp 6.
         if (lane == 0) {
-            const uint32_t id_s = idesc_f16(128, 64, bf16, false, false);
-            const uint32_t id_pv = idesc_f16(128, 256, bf16, false, true);
-            int g = 0, ks = 0;
+            const int c = warp == 8 ? 0 : 1;
+            const uint32_t id_s = idesc_f16(128, NT, bf16, false, false);
+            int g = 0, nq = 0, prev_key = -1;
             bool stop = false;
-            for (int u = w_beg; u < w_end && !stop; ++u) {
-                const int w = u / kp.head_groups;
-                const SplitInfo s = split_info(kp, sp, w);
-                if (!mbar_wait(bar(B_Q_FULL), ks & 1, abort_flag)) break;
-                fence_proxy_async_smem();       // cp.async (generic proxy) writes -> tensor-core reads
-                tc_fence_after();
-                int ns = 0, npv = 0;             // next tile to issue S / P.V for
-                uint64_t t_idle = 0;
-                while (npv < s.ntiles) {
-                    bool progressed = false;
-                    if (ns < s.ntiles) {
-                        const int gi = g + ns, st = gi & 1;
-                        if (mbar_test(bar(B_KV_FULL + st), (gi >> 1) & 1) &&
-                            (gi < 2 || mbar_test(bar(B_S_FREE + st), ((gi >> 1) - 1) & 1))) {
-                            fence_proxy_async_smem();
-                            tc_fence_after();
-                            const uint32_t d = tmem + TM_S + st * 64;
-                            const uint32_t kv = sb + KV_OFF + st * KV_STAGE;
+            Unit cur = u_beg < u_end ? unit_info(kp, sp, u_beg) : Unit{};
+            for (int u = u_beg; u < u_end && !stop; ++u) {
+                const Unit nxt = u + 1 < u_end ? unit_info(kp, sp, u + 1) : cur;
+                const Unit &s = cur;
+                const bool next_reloads = u + 1 < u_end && nxt.key != s.key;
+                if (s.key != prev_key) {
+                    if (!mbar_wait(bar(B_Q_FULL), nq & 1, abort_flag)) break;
+                    ++nq;
+                    prev_key = s.key;
+                }
+                for (int i = 0; i < s.ntiles; ++i) {
+                    const int gi = g + i, st = gi & (kStages - 1), use = gi / kStages;
+                    if (!mbar_wait(bar(B_KV_FULL + st), use & 1, abort_flag) ||
+                        (use >= 1 && !mbar_wait(bar(B_S_FREE + st), (use - 1) & 1, abort_flag))) {
+                        stop = true;
+                        break;
+                    }
+                    fence_proxy_async_smem();    // cp.async (generic proxy) writes -> tensor-core reads
+                    tc_fence_after();
+                    const uint32_t d = tmem + TM_S + st * 2 * NT + c * NT;
+                    const uint32_t kv = sb + KV_OFF + st * KV_STAGE;
 #pragma unroll 8
-                            for (int k = 0; k < 32; ++k) {
-                                const uint32_t off = (k >> 2) * 8192u + (k & 3) * 32u;
-                                umma_f16(d, sdesc_sw128(sb + Q_OFF + off, 16, 1024),
-                                         sdesc_sw128(kv + off, 16, 1024), id_s, k > 0);
-                            }
-                            umma_commit(bar(B_S_FULL + st));
-                            if (ns == s.ntiles - 1) umma_commit(bar(B_Q_EMPTY));
-                            ++ns;
-                            progressed = true;
-                        }
+                    for (int k = 0; k < 16; ++k) {
+                        const uint32_t kk = c * 16 + k, blk = kk >> 2, sub = (kk & 3) * 32u;
+                        umma_f16(d, sdesc_sw128(sb + Q_OFF + blk * 8192u + sub, 16, 1024),
+                                 sdesc_sw128(kv + blk * KV_BLOCK + sub, 16, 1024), id_s, k > 0);
                     }
-                    if (npv < ns) {
-                        const int gj = g + npv, st = gj & 1;
-                        if (mbar_test(bar(B_P_FULL), gj & 1) &&
-                            (npv > 0 || ks == 0 || mbar_test(bar(B_O_FREE), (ks - 1) & 1))) {
-                            tc_fence_after();
-                            const uint32_t kv = sb + KV_OFF + st * KV_STAGE;
-#pragma unroll
-                            for (int k = 0; k < 8; ++k) {
-                                const int half = k >> 2, sub = k & 3;
-                                const uint32_t a = sb + P_OFF + (half ? 0u : 8192u) + sub * 32u;
-                                const uint32_t b = kv + half * 32768u + sub * 2048u;
-                                umma_f16(tmem + TM_O, sdesc_sw128(a, 16, 1024), sdesc_sw128(b, 8192, 1024), id_pv,
-                                         !(npv == 0 && k == 0));
-                            }
-                            umma_commit(bar(B_KV_EMPTY + st));
-                            umma_commit(bar(B_O_DONE));
-                            ++npv;
-                            progressed = true;
-                        }
-                    }
-                    if (progressed) {
-                        t_idle = 0;
-                    } else {
-                        if (*abort_flag) { stop = true; break; }
-                        const uint64_t now = globaltimer_ns();
-                        if (t_idle == 0) t_idle = now;
-                        else if (now - t_idle > kTimeoutNs) {
-                            *abort_flag = 1;
-                            stop = true;
-                            break;
-                        }
-                    }
+                    umma_commit(bar(B_S_FULL + st));
+                    if (i == s.ntiles - 1 && next_reloads) umma_commit(bar(B_Q_EMPTY));
                 }
                 g += s.ntiles;
-                ++ks;
+                cur = nxt;
             }
-            // drain: every MMA issued so far has completed before TMEM is freed
-            umma_commit(bar(B_TEARDOWN));
+            // drain: every MMA this thread issued has completed before TMEM is freed
+            const uint32_t tb = bar(c == 0 ? B_TEARDOWN : B_TEARDOWN_S2);
+            umma_commit(tb);
             const uint64_t t0 = globaltimer_ns();
-            while (!mbar_try_wait(bar(B_TEARDOWN), 0) && globaltimer_ns() - t0 < kTimeoutNs) {
+            while (!mbar_try_wait(tb, 0) && globaltimer_ns() - t0 < kTimeoutNs) {
             }
         }
         __syncwarp();
-    } else if (warp >= 4) {
+    } else if (warp >= 4 && warp < 8) {
         // ======================= softmax / epilogue =======================
         // Warps 4-5 own the score rows (heads) and O[:, 0:256]; warps 6-7 own
         // O[:, 256:512] of the same heads.  Warps 4-5 publish each tile's
-        // rescale factor and the final (max, sum) through one-way mbarriers;
-        // only warps 6-7 wait on them.
+        // rescale factor and the unit's final (max, sum) through one-way
+        // mbarriers; only warps 6-7 wait on them.
         const int r = tid - 128;             // TMEM lane == score row
         const bool head_row = r < 64;
         const int h = r & 63;
-        const uint32_t lane_base = static_cast<uint32_t>((warp - 4) * 32) << 16;
+        const int wl = warp - 4;
+        const uint32_t lane_base = static_cast<uint32_t>(wl * 32) << 16;
         const float sl2 = kp.scale_log2;
-        // epilogue staging: 2 KB per warp in P rows 64..127 (idle during the epilogue)
-        uint8_t *stage = base + P_OFF + 8192u + static_cast<uint32_t>(warp - 4) * 2048u;
+        const uint32_t id_pv = idesc_f16(128, 256, bf16, false, true);
+        uint8_t *stage = base + EPI_OFF + static_cast<uint32_t>(wl) * 1024u;
         int g = 0, ks = 0;
-        for (int u = w_beg; u < w_end; ++u) {
-            const int w = u / kp.head_groups, h0 = (u - w * kp.head_groups) * 64;
-            const int nh = min(64, kp.q_n - h0);
-            const SplitInfo s = split_info(kp, sp, w);
+        bool stop = false;
+        Unit cur = u_beg < u_end ? unit_info(kp, sp, u_beg) : Unit{};
+        for (int u = u_beg; u < u_end && !stop; ++u) {
+            const Unit nxt = u + 1 < u_end ? unit_info(kp, sp, u + 1) : cur;
+            const Unit &s = cur;
+            const bool live_head = head_row && h < s.nh;
             float m = -INFINITY, l = 0.f;
-            bool stop = false;
             for (int i = 0; i < s.ntiles; ++i) {
-                const int gi = g + i, st = gi & 1;
-                if (!warp_wait(bar(B_S_FULL + st), (gi >> 1) & 1, abort_flag)) { stop = true; break; }
-                tc_fence_after();
+                const int gi = g + i, st = gi & (kStages - 1), use = gi / kStages, pb = gi & 1;
                 float alpha = 1.f;
-                uint32_t pw[32];
-                const bool live_head = head_row && h < nh;
+                uint32_t pw[NT / 2];
                 if (head_row) {
-                    uint32_t sv[64];
-                    tmem_ld32(tmem + lane_base + TM_S + st * 64, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
-                    tmem_ld32(tmem + lane_base + TM_S + st * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
-                    tmem_wait_ld();
-                    tc_fence_before();
-                    mbar_arrive(bar(B_S_FREE + st));
-                    if (!warp_wait(bar(B_KV_FULL + st), (gi >> 1) & 1, abort_flag)) { stop = true; break; }
-                    if (live_head) {
-                        const uint32_t v0 = valid_s[st * 2 + 0], v1 = valid_s[st * 2 + 1];
-                        float x[64];
+                    if (!warp_wait(bar(B_S_FULL + st), use & 1, abort_flag)) { stop = true; break; }
+                    tc_fence_after();
+                    uint32_t sv[NT];
+                    {
+                        uint32_t sa[NT / 2], sc[NT / 2];
 #pragma unroll
-                        for (int j = 0; j < 64; ++j) x[j] = __uint_as_float(sv[j]);
-                        if ((v0 & v1) != 0xffffffffu) {
+                        for (int hf = 0; hf < 2; ++hf) {        // the two reduction halves of S, 16 columns at a time
+                            tmem_ld16(tmem + lane_base + TM_S + st * 2 * NT + hf * 16, sa);
+                            tmem_ld16(tmem + lane_base + TM_S + st * 2 * NT + NT + hf * 16, sc);
+                            tmem_wait_ld();
 #pragma unroll
-                            for (int j = 0; j < 64; ++j)
-                                if (!(((j < 32 ? v0 >> j : v1 >> (j - 32)) & 1u))) x[j] = -INFINITY;
+                            for (int j = 0; j < NT / 2; ++j)
+                                sv[hf * 16 + j] = __float_as_uint(__uint_as_float(sa[j]) + __uint_as_float(sc[j]));
                         }
-                        float mx[32];
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(B_S_FREE + st));
+                    // tile i landed before its S was computed; this wait only
+                    // orders the row-mask word
+                    if (!warp_wait(bar(B_KV_FULL + st), use & 1, abort_flag)) { stop = true; break; }
+                    if (live_head) {
+                        const uint32_t vm = valid_s[st];
+                        float x[NT];
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) mx[j] = fmaxf(x[2 * j], x[2 * j + 1]);
+                        for (int j = 0; j < NT; ++j) x[j] = ((vm >> j) & 1u) ? __uint_as_float(sv[j]) : -INFINITY;
+                        float mx[NT / 2];
 #pragma unroll
-                        for (int w2 = 16; w2 >= 1; w2 >>= 1)
+                        for (int j = 0; j < NT / 2; ++j) mx[j] = fmaxf(x[2 * j], x[2 * j + 1]);
+#pragma unroll
+                        for (int w2 = NT / 4; w2 >= 1; w2 >>= 1)
 #pragma unroll
                             for (int j = 0; j < w2; ++j) mx[j] = fmaxf(mx[j], mx[j + w2]);
                         const float tmax = mx[0] * sl2;   // softmax_scale > 0 keeps the arg-max
@@ -388,17 +505,17 @@ __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(KParams kp)
                             alpha = (m == -INFINITY) ? 0.f : fast_exp2(m - tmax);
                             m = tmax;
                         }
-                        float ps[32];
+                        float ps[NT / 2];
                         if (m == -INFINITY) {
 #pragma unroll
-                            for (int j = 0; j < 32; ++j) {
+                            for (int j = 0; j < NT / 2; ++j) {
                                 ps[j] = 0.f;
                                 pw[j] = 0u;
                             }
                         } else {
                             const float nm = -m;
 #pragma unroll
-                            for (int j = 0; j < 32; ++j) {
+                            for (int j = 0; j < NT / 2; ++j) {
                                 const float p0 = fast_exp2(fmaf(x[2 * j], sl2, nm));
                                 const float p1 = fast_exp2(fmaf(x[2 * j + 1], sl2, nm));
                                 ps[j] = p0 + p1;
@@ -406,22 +523,23 @@ __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(KParams kp)
                             }
                         }
 #pragma unroll
-                        for (int w2 = 16; w2 >= 1; w2 >>= 1)
+                        for (int w2 = NT / 4; w2 >= 1; w2 >>= 1)
 #pragma unroll
                             for (int j = 0; j < w2; ++j) ps[j] += ps[j + w2];
                         l = l * alpha + ps[0];
                     }
-                    alpha_s[(gi & 1) * 64 + r] = alpha;
-                    mbar_arrive(bar(B_ALPHA + (gi & 1)));
+                    alpha_s[st * 64 + r] = alpha;
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(B_ALPHA + st));
                 } else {
-                    tc_fence_before();
-                    mbar_arrive(bar(B_S_FREE + st));
-                    if (!warp_wait(bar(B_ALPHA + (gi & 1)), (gi >> 1) & 1, abort_flag)) { stop = true; break; }
-                    alpha = alpha_s[(gi & 1) * 64 + h];
+                    if (!warp_wait(bar(B_ALPHA + st), use & 1, abort_flag)) { stop = true; break; }
+                    alpha = alpha_s[st * 64 + h];
                 }
-                if (gi >= 1 && !warp_wait(bar(B_O_DONE), (gi - 1) & 1, abort_flag)) { stop = true; break; }
-                tc_fence_after();
+                // rescale this warp's half of O once P.V(i-1) has landed in it
                 if (i > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+                    const int gp = gi - 1;
+                    if (!warp_wait(bar(B_O_DONE + (gp & 1)), (gp >> 1) & 1, abort_flag)) { stop = true; break; }
+                    tc_fence_after();
 #pragma unroll 1
                     for (int c = 0; c < 8; ++c) {
                         uint32_t o[32];
@@ -433,127 +551,148 @@ __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(KParams kp)
                     }
                     tmem_wait_st();
                 }
-                // the previous split's epilogue staged O through P rows 64..127:
-                // all four warps must be done with it before a new P lands there
-                if (i == 0 && ks > 0 && head_row && !warp_wait(bar(B_O_FREE), (ks - 1) & 1, abort_flag)) {
-                    stop = true;
-                    break;
-                }
-                if (live_head) {
-                    uint8_t *prow = base + P_OFF;
+                if (head_row) {
+                    // P buffer pb was last read by P.V(i-2)
+                    if (gi >= 2 && !warp_wait(bar(B_O_DONE + pb), ((gi - 2) >> 1) & 1, abort_flag)) {
+                        stop = true;
+                        break;
+                    }
+                    if (live_head) {
 #pragma unroll
-                    for (int c = 0; c < 8; ++c)
-                        *reinterpret_cast<uint4 *>(prow + sw128(64 + r, c)) =
-                            make_uint4(pw[4 * c], pw[4 * c + 1], pw[4 * c + 2], pw[4 * c + 3]);
+                        for (int c = 0; c < NT / 8; ++c)
+                            *reinterpret_cast<uint4 *>(base + P_OFF + sw128(64 + r, pb * 4 + c)) =
+                                make_uint4(pw[4 * c], pw[4 * c + 1], pw[4 * c + 2], pw[4 * c + 3]);
+                    }
+                    fence_proxy_async_smem();
                 }
-                fence_proxy_async_smem();
                 tc_fence_before();
-                mbar_arrive(bar(B_P_FULL));
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(B_P_FULL + pb));
+                if (warp == 6) {
+                    // P.V(i) once all four warps have written P(i) / rescaled O
+                    if (lane == 0) {
+                        if (mbar_wait(bar(B_P_FULL + pb), (gi >> 1) & 1, abort_flag)) {
+                            tc_fence_after();
+                            const uint32_t kv = sb + KV_OFF + st * KV_STAGE;
+#pragma unroll
+                            for (int k = 0; k < 4; ++k) {
+                                const uint32_t half = k >> 1, sub = k & 1;
+                                const uint32_t a = sb + P_OFF + (half ? 0u : 8192u) + pb * 64u + sub * 32u;
+                                const uint32_t b = kv + half * 4u * KV_BLOCK + sub * 2048u;
+                                umma_f16(tmem + TM_O, sdesc_sw128(a, 16, 1024), sdesc_sw128(b, KV_BLOCK, 1024), id_pv,
+                                         !(i == 0 && k == 0));
+                            }
+                            umma_commit(bar(B_KV_EMPTY + st));
+                            umma_commit(bar(B_O_DONE + pb));
+                        }
+                    }
+                    __syncwarp();
+                    if (*abort_flag) { stop = true; break; }
+                }
             }
             if (stop) break;
             // ---------------- epilogue ----------------
             const int gl = g + s.ntiles - 1;
-            if (!warp_wait(bar(B_O_DONE), gl & 1, abort_flag)) break;
+            if (!warp_wait(bar(B_O_DONE + (gl & 1)), (gl >> 1) & 1, abort_flag)) break;
             tc_fence_after();
             float mm = m, ll = l;
             if (head_row) {
                 stats_s[2 * r] = m;
                 stats_s[2 * r + 1] = l;
-                mbar_arrive(bar(B_STATS));
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(B_STATS));
             } else {
                 if (!warp_wait(bar(B_STATS), ks & 1, abort_flag)) break;
                 mm = stats_s[2 * h];
                 ll = stats_s[2 * h + 1];
             }
             const bool final_split = s.nsplit == 1;
-            const bool ws_ok = final_split || w < kp.ws_capacity_splits;
+            const bool ws_ok = final_split || s.w < kp.ws_capacity_splits;
             if (!ws_ok && r == 0) set_status(kp, SFM_STATUS_WORKSPACE_OVERFLOW);
             float inv = 0.f;
             if (ll > 0.f) {
                 float den = ll;
-                if (final_split && kp.sinks) den += exp2f(__ldg(kp.sinks + h0 + h) * 1.4426950408889634f - mm);
+                if (final_split && kp.sinks) den += exp2f(__ldg(kp.sinks + s.h0 + h) * 1.4426950408889634f - mm);
                 inv = 1.f / den;
             }
-            // Coalesced stores: each thread parks its row chunk in its warp's
-            // staging slice (64 B per row, 16-byte pieces rotated by row), then
-            // lane L writes piece L%4 of row 8k + L/4: a warp store covers
-            // eight whole 64-byte row segments.
-            const int wl = warp - 4;
-            const int srow = lane >> 2, spiece = lane & 3;
-            auto rd_row = [&](int k) { return k * 8 + srow; };          // local row read back by this lane
-            auto row_head = [&](int lr) { return (wl * 32 + lr) & 63; };
-            auto row_dcol = [&](int lr) { return (wl * 32 + lr) < 64 ? 0 : 256; };
-            if (final_split) {
-                uint16_t *obase = static_cast<uint16_t *>(kp.out) + ((int64_t)s.t * kp.q_n + h0) * 512;
+            // O out of TMEM, normalised and packed to 16 bits (the output
+            // dtype for a final split, bf16 for a partial), in two halves of
+            // 128 columns; each half is written out through the warp's
+            // staging slice.  Coalesced stores: each lane parks 32 bytes of its
+            // row (16-byte pieces rotated by lane), then lane L writes piece
+            // L%2 of row 16k + L/2: one warp store covers sixteen 32-byte row
+            // segments (whole sectors).
+            const bool out_bf16 = final_split ? bf16 : true;
+            uint16_t *obase = nullptr;
+            if (final_split) obase = static_cast<uint16_t *>(kp.out) + ((int64_t)s.t * kp.q_n + s.h0) * 512;
+            else if (ws_ok) obase = kp.ws_o + ((int64_t)s.w * kp.q_n + s.h0) * 512;
+            const int srow = lane >> 1, spiece = lane & 1;
+            const int dcol = head_row ? 0 : 256;
 #pragma unroll 1
-                for (int c = 0; c < 8; ++c) {                    // 32 columns per chunk
+            for (int hf = 0; hf < 2; ++hf) {
+                uint32_t pk[64];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
                     uint32_t o[32];
-                    __syncwarp();
-                    tmem_ld32(tmem + lane_base + TM_O + c * 32, o);
+                    tmem_ld32(tmem + lane_base + TM_O + (hf * 4 + c) * 32, o);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const int j = q * 8;
-                        *reinterpret_cast<uint4 *>(stage + lane * 64 + ((q ^ (lane & 3)) << 4)) = make_uint4(
-                            pack2(__uint_as_float(o[j]) * inv, __uint_as_float(o[j + 1]) * inv, bf16),
-                            pack2(__uint_as_float(o[j + 2]) * inv, __uint_as_float(o[j + 3]) * inv, bf16),
-                            pack2(__uint_as_float(o[j + 4]) * inv, __uint_as_float(o[j + 5]) * inv, bf16),
-                            pack2(__uint_as_float(o[j + 6]) * inv, __uint_as_float(o[j + 7]) * inv, bf16));
-                    }
-                    __syncwarp();
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const int lr = rd_row(k), hh = row_head(lr);
-                        const uint4 v = *reinterpret_cast<const uint4 *>(stage + lr * 64 + ((spiece ^ (lr & 3)) << 4));
-                        if (hh < nh)
-                            *reinterpret_cast<uint4 *>(obase + (int64_t)hh * 512 + row_dcol(lr) + c * 32 + spiece * 8) = v;
-                    }
+                    for (int j = 0; j < 16; ++j)
+                        pk[c * 16 + j] = pack2(__uint_as_float(o[2 * j]) * inv, __uint_as_float(o[2 * j + 1]) * inv,
+                                               out_bf16);
                 }
-            } else if (ws_ok) {
-                float *wbase = kp.ws_o + ((int64_t)w * kp.q_n + h0) * 512;
-#pragma unroll 1
-                for (int c = 0; c < 16; ++c) {                   // 16 columns per chunk
-                    uint32_t o[16];
-                    __syncwarp();
-                    tmem_ld16(tmem + lane_base + TM_O + c * 16, o);
-                    tmem_wait_ld();
+                // after the second half, TMEM is free for the next unit once
+                // this warp's next P arrival (which follows this fence) completes
+                if (hf == 1) tc_fence_before();
+                if (!obase) continue;
 #pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        *reinterpret_cast<float4 *>(stage + lane * 64 + ((q ^ (lane & 3)) << 4)) = make_float4(
-                            __uint_as_float(o[4 * q]) * inv, __uint_as_float(o[4 * q + 1]) * inv,
-                            __uint_as_float(o[4 * q + 2]) * inv, __uint_as_float(o[4 * q + 3]) * inv);
+                for (int c = 0; c < 8; ++c) {                    // 16 columns per round
                     __syncwarp();
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const int lr = rd_row(k), hh = row_head(lr);
-                        const float4 v = *reinterpret_cast<const float4 *>(stage + lr * 64 + ((spiece ^ (lr & 3)) << 4));
-                        if (hh < nh)
-                            *reinterpret_cast<float4 *>(wbase + (int64_t)hh * 512 + row_dcol(lr) + c * 16 + spiece * 4) = v;
+                    for (int q = 0; q < 2; ++q)
+                        *reinterpret_cast<uint4 *>(stage + lane * 32 + ((q ^ (lane & 1)) << 4)) =
+                            make_uint4(pk[c * 8 + 4 * q], pk[c * 8 + 4 * q + 1], pk[c * 8 + 4 * q + 2],
+                                       pk[c * 8 + 4 * q + 3]);
+                    __syncwarp();
+#pragma unroll
+                    for (int k = 0; k < 2; ++k) {
+                        const int lr = k * 16 + srow, hh = (wl & 1) * 32 + lr;
+                        const uint4 v = *reinterpret_cast<const uint4 *>(stage + lr * 32 + ((spiece ^ (lr & 1)) << 4));
+                        if (hh < s.nh)
+                            *reinterpret_cast<uint4 *>(obase + (int64_t)hh * 512 + dcol + hf * 128 + c * 16 +
+                                                       spiece * 8) = v;
                     }
                 }
             }
             __syncwarp();
-            if (head_row && h < nh && ws_ok) {
+            if (head_row && h < s.nh && ws_ok) {
                 const float lse = ll > 0.f ? (mm + log2f(ll)) * 0.6931471805599453f : -INFINITY;
-                const int64_t row = (int64_t)s.t * kp.q_n + h0 + h;
                 if (final_split) {
-                    if (kp.lse) kp.lse[row] = lse;
+                    if (kp.lse) kp.lse[(int64_t)s.t * kp.q_n + s.h0 + h] = lse;
                 } else {
-                    kp.ws_lse[(int64_t)w * kp.q_n + h0 + h] = lse;
+                    kp.ws_lse[(int64_t)s.w * kp.q_n + s.h0 + h] = lse;
                 }
             }
-            tc_fence_before();
-            mbar_arrive(bar(B_O_FREE));
             g += s.ntiles;
             ++ks;
+            cur = nxt;
         }
     }
+
+    if (warp == 6 && lane == 0) {
+        // every P.V issued by this thread has completed before TMEM is freed
+        umma_commit(bar(B_TEARDOWN_PV));
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_try_wait(bar(B_TEARDOWN_PV), 0) && globaltimer_ns() - t0 < kTimeoutNs) {
+        }
+    }
+    __syncwarp();
 
     // ---------------- teardown ----------------
     tc_fence_before();
     __syncthreads();
     if (tid == 0 && *abort_flag) set_status(kp, SFM_STATUS_TIMEOUT);
-    if (warp == 2) {
+    if (warp == 8) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }

@@ -1,7 +1,7 @@
 // sfm_combine.cu -- merge the split-KV partial results of each query row.
 //
 // For a row whose attended positions were cut into splits s = 0..n-1 with
-// normalised partial outputs O_s and partial LSEs lse_s:
+// normalised partial outputs O_s (stored as bf16) and partial LSEs lse_s (fp32):
 //   LSE = log sum_s exp(lse_s)                         (the row's log-sum-exp)
 //   O   = sum_s exp(lse_s - LSE) O_s / (1 + exp(sink - LSE))
 // The sink term is the per-head logit added once to the softmax denominator;
@@ -80,15 +80,17 @@ __global__ void __launch_bounds__(kThreads) sfm_combine_kernel(KParams kp)
             const float wl = lane < cn ? expf(kp.ws_lse[(int64_t)(s0 + c + lane) * kp.q_n + h] - L) : 0.f;
             for (int s = 0; s < cn; ++s) {
                 const float w = __shfl_sync(0xffffffffu, wl, s);
-                const float4 *src = reinterpret_cast<const float4 *>(
+                const uint4 *src = reinterpret_cast<const uint4 *>(
                     kp.ws_o + ((int64_t)(s0 + c + s) * kp.q_n + h) * 512 + lane * 16);
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const float4 v = src[q];
-                    acc[4 * q + 0] = fmaf(w, v.x, acc[4 * q + 0]);
-                    acc[4 * q + 1] = fmaf(w, v.y, acc[4 * q + 1]);
-                    acc[4 * q + 2] = fmaf(w, v.z, acc[4 * q + 2]);
-                    acc[4 * q + 3] = fmaf(w, v.w, acc[4 * q + 3]);
+                for (int q = 0; q < 2; ++q) {
+                    const uint4 v = src[q];
+                    const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {      // bf16 pair -> two floats (exact)
+                        acc[8 * q + 2 * e] = fmaf(w, __uint_as_float(wv[e] << 16), acc[8 * q + 2 * e]);
+                        acc[8 * q + 2 * e + 1] = fmaf(w, __uint_as_float(wv[e] & 0xffff0000u), acc[8 * q + 2 * e + 1]);
+                    }
                 }
             }
         }

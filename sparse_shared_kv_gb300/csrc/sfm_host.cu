@@ -9,6 +9,7 @@
 #include <math.h>
 #include <string.h>
 
+
 #include "sfm_internal.cuh"
 
 namespace sfm {
@@ -141,8 +142,12 @@ int make_plan(const sfm_params &p, Plan *pl)
     pl->G = sms;
     pl->T = num_tokens(p);
     const bool decode_like = p.max_seqlen_q <= 16;
-    // tensor-core tiles are 64 rows: splits of 3 tiles
-    pl->split_rows = decode_like ? (pl->path == PATH_TC ? 192 : 256) : (1 << 30);
+    // Tensor-core tiles are 32 rows.  Up to 64 heads: splits of 5 tiles.  128
+    // heads: each split is two work units and writes twice the partial bytes,
+    // so splits are larger (16 tiles).
+    int split = 256;
+    if (pl->path == PATH_TC) split = p.num_heads_q > 64 ? 512 : 160;
+    pl->split_rows = decode_like ? split : (1 << 30);
     const int64_t mp = max_positions(p);
     pl->max_splits_per_token = decode_like ? (mp + pl->split_rows - 1) / pl->split_rows : 1;
     return SFM_OK;
@@ -168,7 +173,7 @@ uint32_t fingerprint(const sfm_params &p, const Plan &pl)
 
 size_t ws_lse_offset(const sfm_params &p, int64_t cap)
 {
-    size_t o = (size_t)cap * p.num_heads_q * 512 * sizeof(float);
+    size_t o = (size_t)cap * p.num_heads_q * 512 * sizeof(uint16_t);
     return (o + 255) & ~(size_t)255;
 }
 
@@ -376,7 +381,7 @@ int sfm_forward(const sfm_params *params, const sfm_tensors *in, const int32_t *
     if (need) {
         const int64_t cap = pl.T * pl.max_splits_per_token;
         kp.ws_capacity_splits = cap;
-        kp.ws_o = static_cast<float *>(workspace);
+        kp.ws_o = static_cast<uint16_t *>(workspace);
         kp.ws_lse = reinterpret_cast<float *>(static_cast<char *>(workspace) + ws_lse_offset(p, cap));
     }
     cudaStream_t st = (cudaStream_t)stream;

@@ -37,6 +37,18 @@ enum MetaHeader {
 // whatever its length, so splits are balanced first by count, then by rows
 constexpr int kSplitOverheadRows = 128;
 
+// A row with n attended positions gets ceil(n / S) splits of equal size
+// (rounded up to 32 rows; never more than S when S is a multiple of 32, so
+// the last split is never empty).  Depends on the row's own n and the params
+// only, which keeps results batch invariant.
+__host__ __device__ inline int split_size(int64_t n, int S)
+{
+    if (n <= 0) return S;
+    const int64_t ns = (n + S - 1) / S;
+    const int64_t sz = (n + ns - 1) / ns;
+    return (int)((sz + 31) & ~(int64_t)31);
+}
+
 __host__ __device__ inline int64_t meta_ws_off() { return kHdr; }
 __host__ __device__ inline int64_t meta_split_off(int G) { return kHdr + (int64_t)G + 1; }
 __host__ __device__ inline int64_t meta_cost_off(int G, int T) { return kHdr + (int64_t)G + 1 + (int64_t)T + 1; }
@@ -67,7 +79,8 @@ struct KParams {
     float scale_log2;                       // softmax_scale * log2(e)
     // plan
     int32_t G, split_rows, fingerprint, path;
-    int32_t head_groups;                    // work units per split (groups of 64 heads, tensor-core path)
+    int32_t head_groups;                    // groups of 64 heads (tensor-core path; 1 otherwise): a token
+                                            // with n splits owns head_groups * n work units, group-major
     int64_t ws_capacity_splits;
     int64_t wcap;                           // capacity of the split -> row map
     // tensors
@@ -80,7 +93,7 @@ struct KParams {
     int32_t *meta_w;
     void *out;
     float *lse;
-    float *ws_o;      // [capacity][q_n][512] normalised partial O
+    uint16_t *ws_o;   // [capacity][q_n][512] normalised partial O, bf16
     float *ws_lse;    // [capacity][q_n] partial LSE
     int32_t *status;
     int32_t *dbg_rows;

@@ -5,7 +5,7 @@
 // 功能说明 and the metadata row of 参数说明).  Here it is one CTA that reads the
 // length tensors on the device (no host round trip) and writes:
 //   * per query row t: its attended-position count n_t cut into
-//     ceil(n_t / split_rows) splits -- a function of the row's own count and
+//     ceil(n_t / split_rows) equal splits -- a function of the row's own count and
 //     the params only, so a row's arithmetic never depends on the rest of the
 //     batch (the 确定性计算 section makes batch invariance the default);
 //   * per query row: the lengths / window / position counts the attention
@@ -159,8 +159,10 @@ __global__ void __launch_bounds__(kPlanThreads) sfm_plan_kernel(KParams kp)
     __syncthreads();
 
     // 3. worker ranges over work units: a unit is one split for one group of
-    //    heads (head_groups units per split, consecutive); worker c starts at
-    //    the first unit whose cumulative cost reaches c / G of the total
+    //    heads; row t owns units [sp[t] * HG, sp[t+1] * HG), group-major, so
+    //    that consecutive units of a worker mostly share their Q rows.  Worker
+    //    c starts at the first unit whose cumulative cost reaches c / G of the
+    //    total.
     const int32_t *xsp = in_smem ? s_sp : sp;
     const int32_t *xcp = in_smem ? s_cp : cp;
     const int64_t HG = kp.head_groups;
@@ -186,7 +188,9 @@ __global__ void __launch_bounds__(kPlanThreads) sfm_plan_kernel(KParams kp)
             } else {
                 const int64_t nu = (int64_t)(xsp[lo + 1] - xsp[lo]) * HG;
                 const int64_t within = target - (int64_t)xcp[lo] * HG;
-                int64_t k = (within + S + kSplitOverheadRows - 1) / (S + kSplitOverheadRows);
+                const int64_t ucost = split_size(in_smem ? (int64_t)s_n[lo] : row_positions(rec, lo), S) +
+                                      kSplitOverheadRows;
+                int64_t k = (within + ucost - 1) / ucost;
                 if (k > nu) k = nu;
                 u = (int64_t)xsp[lo] * HG + k;
             }
