@@ -257,9 +257,11 @@ __global__ void __launch_bounds__(kThreads) sfm_attn_simt_kernel(KParams kp)
                 if (tid == 0 && kp.lse) kp.lse[row] = l > 0.f ? m + logf(l) : -INFINITY;
             } else {
                 const float inv = l > 0.f ? 1.f / l : 0.f;
-                uint16_t *o = kp.ws_o + ((int64_t)w * kp.q_n + hh) * 512;
-                o[tid] = float_to_half(acc[h][0] * inv, SFM_DTYPE_BF16);
-                o[tid + 256] = float_to_half(acc[h][1] * inv, SFM_DTYPE_BF16);
+                // chunk-major partial: [split][dim / 8][head][8]
+                uint16_t *o = kp.ws_o + (int64_t)w * kp.q_n * 512;
+                const int d0 = tid, d1 = tid + 256;
+                o[((int64_t)(d0 >> 3) * kp.q_n + hh) * 8 + (d0 & 7)] = float_to_half(acc[h][0] * inv, SFM_DTYPE_BF16);
+                o[((int64_t)(d1 >> 3) * kp.q_n + hh) * 8 + (d1 & 7)] = float_to_half(acc[h][1] * inv, SFM_DTYPE_BF16);
                 if (tid == 0) kp.ws_lse[(int64_t)w * kp.q_n + hh] = l > 0.f ? m + logf(l) : -INFINITY;
             }
         }

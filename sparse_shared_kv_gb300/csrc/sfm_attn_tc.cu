@@ -8,7 +8,7 @@
 // changes.  Per 32-row KV tile of a unit:
 //   resolver warp 9      resolves the attended rows (window / compressed /
 //                        indices through the block tables) up to 16 tiles
-//                        ahead, four tiles per batch so that a batch costs
+//                        ahead, eight tiles per batch so that a batch costs
 //                        two dependent memory round trips, into a ring of
 //                        row numbers in shared memory;
 //   producer warps 0-3   stream each tile's 32 rows (1 KB each, 8 rows per
@@ -73,19 +73,23 @@ constexpr int kThreads = 384;               // 12 warps: three warpgroups
 constexpr int kProducers = 4;               // KV copy warps
 constexpr uint32_t Q_OFF = 0;                // 8 blocks x 64 rows x 128 B
 constexpr uint32_t P_OFF = 65536;            // 192 rows x 128 B: [0..63] zero, [64..127] P, [128..191] zero
-constexpr uint32_t KV_OFF = 90112;           // 4 stages x 32 KB
-constexpr uint32_t KV_BLOCK = NT * 128;      // one 64-column block of a stage
-constexpr uint32_t KV_STAGE = 8 * KV_BLOCK;
+constexpr uint32_t KV_OFF = 90112;           // 4 stages x 32 KB, column-block major (below)
+constexpr uint32_t KV_BLOCK = NT * 128;      // one 64-column block of one stage (32 rows)
+constexpr uint32_t KV_STAGE = 8 * KV_BLOCK;  // bytes of one stage
+constexpr uint32_t KV_COL = kStages * KV_BLOCK;   // stride between 64-column blocks
+// Column block a of stage st sits at KV_OFF + a * KV_COL + st * KV_BLOCK, so
+// stages 2j and 2j+1 form one contiguous 64-row operand per column block.
+__host__ __device__ constexpr uint32_t kv_at(uint32_t st, uint32_t a) { return KV_OFF + a * KV_COL + st * KV_BLOCK; }
 constexpr uint32_t MISC_OFF = KV_OFF + kStages * KV_STAGE;   // 221184
 constexpr uint32_t MISC_BYTES = 4608;
 constexpr uint32_t EPI_OFF = MISC_OFF + MISC_BYTES;          // epilogue staging, 1 KB per softmax warp
 constexpr uint32_t kSmemBytes = EPI_OFF + 4 * 1024 + 1024;   // + alignment slack
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t TM_O = 0;                 // O: columns [0, 256)
-constexpr uint32_t TM_S = 256;               // S buffer s: [256 + 64 s, 320 + 64 s), two 32-column halves
+constexpr uint32_t TM_S = 256;               // S: chain c, stage s at [256 + 128 c + 32 s, +32)
 constexpr float kRescaleThreshold = 8.0f;    // log2 units
 constexpr int kRing = 16;                    // resolved tiles in flight
-constexpr int kResolveBatch = 4;             // tiles per resolver batch
+constexpr int kResolveBatch = 8;             // tiles per resolver batch
 
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 static_assert(P_OFF == Q_OFF + 8 * 8192, "the last Q block's alias rows must be P's leading zero rows");
@@ -123,17 +127,17 @@ struct Unit {
     Tok k;
 };
 
-// Unit u of the plan: its query row, split, head group and row range.  Two
-// dependent loads (split -> row -> row record) instead of a search and a
-// length walk.
-__device__ __forceinline__ Unit unit_info(const KParams &kp, const int32_t *sp, int u)
+// Unit u of the plan from its split's 64-byte record (query row, first split
+// and split count of the row, the row's split size and lengths / window /
+// position counts): the split, head group and row range of the unit.
+__device__ __forceinline__ Unit unit_decode(const KParams &kp, int4 r0, int4 r1, int4 r2, int u)
 {
     Unit s;
     const int HG = kp.head_groups;
-    s.t = __ldg(kp.meta + meta_own_off(kp.G, kp.T) + u / HG);
-    const int32_t *rec = kp.meta + meta_rec_off(kp.G, kp.T) + (int64_t)kRecWords * s.t;
-    const int s_beg = __ldg(sp + s.t), s_end = __ldg(sp + s.t + 1);
-    s.nsplit = s_end - s_beg;
+    s.t = r0.x;
+    const int s_beg = r0.y;
+    s.nsplit = r0.z;
+    const int size = r0.w;
     const int local = u - s_beg * HG;
     const int hg = s.nsplit > 0 ? local / s.nsplit : 0;
     const int sidx = local - hg * s.nsplit;
@@ -142,25 +146,30 @@ __device__ __forceinline__ Unit unit_info(const KParams &kp, const int32_t *sp, 
     s.nh = min(64, kp.q_n - s.h0);
     s.key = s.t * HG + hg;
     Tok &k = s.k;
-    k.b = __ldg(rec + 0);
-    k.kv_len = __ldg(rec + 1);
-    k.cmp_len = __ldg(rec + 2);
-    k.p_cmp = __ldg(rec + 3);
-    k.lo = __ldg(rec + 4);
-    k.hi = __ldg(rec + 5);
-    k.n_ori = __ldg(rec + 6);
-    k.n_cmp = __ldg(rec + 7);
+    k.b = r1.x;
+    k.kv_len = r1.y;
+    k.cmp_len = r1.z;
+    k.p_cmp = r1.w;
+    k.lo = r2.x;
+    k.hi = r2.y;
+    k.n_ori = r2.z;
+    k.n_cmp = r2.w;
     k.i = 0;
     k.q_len = 0;
     k.p = 0;
     k.valid = 1;
     const int n = k.n_ori + k.n_cmp;
-    const int size = split_size(n, kp.split_rows);
     s.pos0 = sidx * size;
     s.pos1 = min(n, s.pos0 + size);
     const int rows = s.pos1 > s.pos0 ? s.pos1 - s.pos0 : 0;
     s.ntiles = rows > 0 ? (rows + NT - 1) / NT : 1;   // an empty split still runs one masked tile
     return s;
+}
+
+__device__ __forceinline__ Unit unit_info(const KParams &kp, const int32_t *srec, int u)
+{
+    const int4 *r = reinterpret_cast<const int4 *>(srec + (int64_t)(u / kp.head_groups) * kSrecWords);
+    return unit_decode(kp, __ldg(r), __ldg(r + 1), __ldg(r + 2), u);
 }
 
 __device__ __forceinline__ uint32_t pack2(float a, float b, bool bf16)
@@ -175,28 +184,32 @@ __device__ __forceinline__ uint32_t pack2(float a, float b, bool bf16)
 
 // Row entries of this lane's row in tiles i0 .. i0+K-1 of the unit: -1 for a
 // skipped or masked position, else the pool row with bit 31 set for the
-// compressed pool.  Same rules and status bits as resolve_row(); every index
-// load of the batch is issued before any block-table load.
+// compressed pool.  Same rules and status bits as resolve_row().  Every load
+// is unconditional, from the real address or from an always-valid one, so
+// that the K index loads and then the K block-table loads each go out back to
+// back: a batch costs two memory round trips whatever K is.
 template <int K>
 __device__ __forceinline__ void resolve_tiles(const KParams &kp, const Unit &s, int i0, int lane, int32_t (&ent)[K])
 {
     const Tok &k = s.k;
+    const int32_t *safe = kp.meta;      // any readable int32
     int e[K];
     bool in[K], cmp[K];
+    // 1. positions -> logical rows (the index tensors for top-k sources)
 #pragma unroll
     for (int j = 0; j < K; ++j) {
         const int pos = s.pos0 + (i0 + j) * NT + lane;
         in[j] = pos < s.pos1;
         cmp[j] = pos >= k.n_ori;
         const int jj = pos - k.n_ori;
-        e[j] = cmp[j] ? jj : k.lo + pos;
-        if (in[j]) {
-            if (!cmp[j] && kp.ori_topk > 0) e[j] = __ldg(kp.ori_idx + (int64_t)s.t * kp.ori_topk + pos);
-            else if (cmp[j] && kp.cmp_topk > 0) e[j] = __ldg(kp.cmp_idx + (int64_t)s.t * kp.cmp_topk + jj);
-        }
+        const bool from_idx = in[j] && (cmp[j] ? kp.cmp_topk > 0 : kp.ori_topk > 0);
+        const int32_t *ip = !from_idx ? safe
+                            : cmp[j]  ? kp.cmp_idx + (int64_t)s.t * kp.cmp_topk + jj
+                                      : kp.ori_idx + (int64_t)s.t * kp.ori_topk + pos;
+        const int v = __ldg(ip);
+        e[j] = from_idx ? v : (cmp[j] ? jj : k.lo + pos);
     }
     int err = 0;
-    int64_t row[K];
 #pragma unroll
     for (int j = 0; j < K; ++j) {
         bool ok = in[j];
@@ -209,7 +222,35 @@ __device__ __forceinline__ void resolve_tiles(const KParams &kp, const Unit &s, 
                  (kp.cmp_mask_mode != 3 || (int64_t)(e[j] + 1) * kp.cmp_ratio <= (int64_t)k.p_cmp + 1);
         }
         in[j] = ok;
-        row[j] = ok ? phys_row(kp, cmp[j] ? 1 : 0, k.b, e[j]) : 0;
+    }
+    // 2. logical rows -> pool rows
+    int64_t row[K];
+    if (kp.layout_kv == SFM_LAYOUT_PAGED) {
+        int32_t blk[K];
+        bool inb[K];
+#pragma unroll
+        for (int j = 0; j < K; ++j) {
+            const int bs = cmp[j] ? kp.cmp_bs : kp.ori_bs;
+            const int bts = cmp[j] ? kp.cmp_bt_stride : kp.ori_bt_stride;
+            const int ee = in[j] ? e[j] : 0;
+            const int bi = ee / bs;
+            inb[j] = in[j] && bi < bts;
+            const int32_t *bp = inb[j] ? (cmp[j] ? kp.cmp_bt : kp.ori_bt) + (int64_t)k.b * bts + bi : safe;
+            blk[j] = __ldg(bp);
+        }
+#pragma unroll
+        for (int j = 0; j < K; ++j) {
+            const int bs = cmp[j] ? kp.cmp_bs : kp.ori_bs;
+            row[j] = (inb[j] && blk[j] >= 0) ? (int64_t)blk[j] * bs + (in[j] ? e[j] : 0) % bs : -1;
+        }
+    } else if (kp.layout_kv == SFM_LAYOUT_TND) {
+        const int64_t base_o = __ldg(kp.cu_ori + k.b);
+        const int64_t base_c = kp.has_cmp ? (int64_t)__ldg(kp.cu_cmp + k.b) : 0;
+#pragma unroll
+        for (int j = 0; j < K; ++j) row[j] = (cmp[j] ? base_c : base_o) + e[j];
+    } else {
+#pragma unroll
+        for (int j = 0; j < K; ++j) row[j] = (int64_t)k.b * (cmp[j] ? kp.cmp_s : kp.ori_s) + e[j];
     }
 #pragma unroll
     for (int j = 0; j < K; ++j) {
@@ -278,13 +319,33 @@ __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(const KParams 
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(base + TMEM_SLOT_OFF);
 
+    // While the planner still runs: pull this CTA's share of the index
+    // tensors, block tables and Q into L2 (they do not depend on the plan),
+    // so the first dependent loads after the plan hit L2.
+    if (tid == 9 * 32) {
+        const int G = gridDim.x, c = blockIdx.x;
+        constexpr int64_t kCap = 256 * 1024;
+        prefetch_share(kp.cmp_idx, (int64_t)kp.T * kp.cmp_topk * 4, c, G, kCap);
+        prefetch_share(kp.ori_idx, (int64_t)kp.T * kp.ori_topk * 4, c, G, kCap);
+        if (kp.layout_kv == SFM_LAYOUT_PAGED) {
+            prefetch_share(kp.ori_bt, (int64_t)kp.batch * kp.ori_bt_stride * 4, c, G, kCap);
+            if (kp.has_cmp) prefetch_share(kp.cmp_bt, (int64_t)kp.batch * kp.cmp_bt_stride * 4, c, G, kCap);
+        }
+        prefetch_share(kp.q, (int64_t)kp.T * kp.q_n * 1024, c, G, kCap);
+    }
+
     // everything above overlapped the planner; the plan is read from here on
     grid_dependency_wait();
+    // one round trip: the header check and this worker's record (its unit
+    // range and its first unit's split record) are independent loads
+    const int32_t *sp = kp.meta + meta_srec_off(kp.G, kp.T, kp.wcap);   // split records
+    const int4 *wr = reinterpret_cast<const int4 *>(kp.meta + meta_wrec_off(kp.G, kp.T, kp.wcap) +
+                                                    (int64_t)blockIdx.x * kWrecWords);
+    const int4 w0 = __ldg(wr), w1 = __ldg(wr + 1), w2 = __ldg(wr + 2), w3 = __ldg(wr + 3);
     const bool ok = meta_ok(kp);
-    const int worker = blockIdx.x;
-    const int32_t *sp = kp.meta + meta_split_off(kp.G);
-    const int u_beg = ok ? __ldg(kp.meta + meta_ws_off() + worker) : 0;
-    const int u_end = ok ? __ldg(kp.meta + meta_ws_off() + worker + 1) : 0;
+    const int u_beg = ok ? w0.x : 0;
+    const int u_end = ok ? w0.y : 0;
+    const Unit first = unit_decode(kp, w1, w2, w3, u_beg);
 
     int32_t *ring = reinterpret_cast<int32_t *>(base + RING_OFF);
 
@@ -295,7 +356,7 @@ __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(const KParams 
         // and publishes each tile's 32 entries in ring slot (tile % kRing).
         int g = 0;
         bool stop = false;
-        Unit cur = u_beg < u_end ? unit_info(kp, sp, u_beg) : Unit{};
+        Unit cur = first;
         for (int u = u_beg; u < u_end && !stop; ++u) {
             const Unit nxt = u + 1 < u_end ? unit_info(kp, sp, u + 1) : cur;   // prefetched
             const Unit &s = cur;
@@ -332,26 +393,31 @@ __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(const KParams 
         const uint8_t *zero_src = static_cast<const uint8_t *>(kp.q);
         int g = 0, nq = 0, prev_key = -1;
         bool stop = false;
-        for (int u = u_beg; u < u_end && !stop; ++u) {
-            const Unit s = unit_info(kp, sp, u);
-            if (s.key != prev_key) {
-                if (nq > 0 && !warp_wait(bar(B_Q_EMPTY), (nq - 1) & 1, abort_flag)) break;
-                const uint8_t *qrow = static_cast<const uint8_t *>(kp.q) + ((int64_t)s.t * kp.q_n + s.h0) * 1024;
+        // the unit's Q rows (16 heads per warp); rows past the group's heads are zero
+        auto copy_q = [&](const Unit &s) -> bool {
+            if (nq > 0 && !warp_wait(bar(B_Q_EMPTY), (nq - 1) & 1, abort_flag)) return false;
+            const uint8_t *qrow = static_cast<const uint8_t *>(kp.q) + ((int64_t)s.t * kp.q_n + s.h0) * 1024;
 #pragma unroll 4
-                for (int rr = 0; rr < 64 / kProducers; ++rr) {
-                    const int hh = pw * (64 / kProducers) + rr;
-                    const bool live = hh < s.nh;
+            for (int rr = 0; rr < 64 / kProducers; ++rr) {
+                const int hh = pw * (64 / kProducers) + rr;
+                const bool live = hh < s.nh;
 #pragma unroll
-                    for (int half = 0; half < 2; ++half) {
-                        const int C = lane + half * 32;
-                        const uint32_t dst = sb + Q_OFF + (C >> 3) * 8192u + sw128(hh, C & 7);
-                        cp_async16(dst, live ? qrow + (int64_t)hh * 1024 + C * 16 : zero_src, live ? 16u : 0u);
-                    }
+                for (int half = 0; half < 2; ++half) {
+                    const int C = lane + half * 32;
+                    const uint32_t dst = sb + Q_OFF + (C >> 3) * 8192u + sw128(hh, C & 7);
+                    cp_async16(dst, live ? qrow + (int64_t)hh * 1024 + C * 16 : zero_src, live ? 16u : 0u);
                 }
-                cp_async_arrive_noinc(bar(B_Q_FULL));
-                ++nq;
-                prev_key = s.key;
             }
+            cp_async_arrive_noinc(bar(B_Q_FULL));
+            ++nq;
+            prev_key = s.key;
+            return true;
+        };
+        Unit cur = first;
+        for (int u = u_beg; u < u_end && !stop; ++u) {
+            const Unit nxt = u + 1 < u_end ? unit_info(kp, sp, u + 1) : cur;   // prefetched
+            const Unit &s = cur;
+            const bool reload = s.key != prev_key;
             for (int i = 0; i < s.ntiles; ++i) {
                 const int gi = g + i, slot = gi % kRing, st = gi & (kStages - 1), use = gi / kStages;
                 if (!warp_wait(bar(B_ROW_FULL + slot), (gi / kRing) & 1, abort_flag)) { stop = true; break; }
@@ -365,7 +431,7 @@ __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(const KParams 
                 }
                 const uint32_t vm = __ballot_sync(0xffffffffu, row != nullptr);
                 if (use >= 1 && !warp_wait(bar(B_KV_EMPTY + st), (use - 1) & 1, abort_flag)) { stop = true; break; }
-                const uint32_t stage = sb + KV_OFF + st * KV_STAGE;
+                const uint32_t stage = sb + kv_at(st, 0);
                 const unsigned long long my_row = reinterpret_cast<unsigned long long>(row);
 #pragma unroll
                 for (int k = 0; k < kRowsPerWarp; ++k) {
@@ -374,7 +440,7 @@ __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(const KParams 
 #pragma unroll
                     for (int half = 0; half < 2; ++half) {
                         const int C = lane + half * 32;
-                        const uint32_t dst = stage + (C >> 3) * KV_BLOCK + sw128(rr, C & 7);
+                        const uint32_t dst = stage + (C >> 3) * KV_COL + sw128(rr, C & 7);
                         cp_async16(dst, src ? src + C * 16 : zero_src, src ? 16u : 0u);
                     }
                 }
@@ -383,8 +449,12 @@ __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(const KParams 
                     valid_s[st] = vm;                        // the tile's row-valid bits
                     mbar_arrive(bar(B_KV_FULL + st));        // release: the word is visible with the phase
                 }
+                // Q after the unit's first tile: the first tile's row
+                // addresses are the longer dependency chain
+                if (i == 0 && reload && !copy_q(s)) { stop = true; break; }
             }
             g += s.ntiles;
+            cur = nxt;
         }
         cp_async_wait<0>();
     } else if (warp == 8 || warp == 10) {
@@ -392,14 +462,18 @@ __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(const KParams 
         // S(i) needs tile i staged and its S buffer free.  Its 32 reduction
         // steps run as two independent accumulation chains issued by two
         // warps: warp 8 over dimensions 0..255, warp 10 over 256..511, into
-        // adjacent 32-column halves of the S buffer; the softmax adds them.
-        // P.V is issued by warp 6.
+        // two TMEM halves (chain c, stage st at TM_S + 128 c + 32 st); the
+        // softmax adds them.  An even tile and the next tile of the same unit
+        // are computed together as one N=64 product, which halves the number
+        // of S instructions (the tensor pipe's instruction rate, not its math,
+        // bounds these small products).  P.V is issued by warp 6.
         if (lane == 0) {
             const int c = warp == 8 ? 0 : 1;
             const uint32_t id_s = idesc_f16(128, NT, bf16, false, false);
+            const uint32_t id_s2 = idesc_f16(128, 2 * NT, bf16, false, false);
             int g = 0, nq = 0, prev_key = -1;
             bool stop = false;
-            Unit cur = u_beg < u_end ? unit_info(kp, sp, u_beg) : Unit{};
+            Unit cur = first;
             for (int u = u_beg; u < u_end && !stop; ++u) {
                 const Unit nxt = u + 1 < u_end ? unit_info(kp, sp, u + 1) : cur;
                 const Unit &s = cur;
@@ -409,25 +483,32 @@ __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(const KParams 
                     ++nq;
                     prev_key = s.key;
                 }
-                for (int i = 0; i < s.ntiles; ++i) {
+                for (int i = 0; i < s.ntiles;) {
                     const int gi = g + i, st = gi & (kStages - 1), use = gi / kStages;
-                    if (!mbar_wait(bar(B_KV_FULL + st), use & 1, abort_flag) ||
-                        (use >= 1 && !mbar_wait(bar(B_S_FREE + st), (use - 1) & 1, abort_flag))) {
+                    // an even tile and the next one of the same unit share one
+                    // 64-row S (stages 2j, 2j+1 are one operand)
+                    const int nt = ((gi & 1) == 0 && i + 1 < s.ntiles) ? 2 : 1;
+                    bool good = true;
+                    for (int j = 0; j < nt && good; ++j)
+                        good = mbar_wait(bar(B_KV_FULL + st + j), use & 1, abort_flag) &&
+                               (use == 0 || mbar_wait(bar(B_S_FREE + st + j), (use - 1) & 1, abort_flag));
+                    if (!good) {
                         stop = true;
                         break;
                     }
                     fence_proxy_async_smem();    // cp.async (generic proxy) writes -> tensor-core reads
                     tc_fence_after();
-                    const uint32_t d = tmem + TM_S + st * 2 * NT + c * NT;
-                    const uint32_t kv = sb + KV_OFF + st * KV_STAGE;
+                    const uint32_t d = tmem + TM_S + c * (kStages * NT) + st * NT;
+                    const uint32_t id = nt == 2 ? id_s2 : id_s;
 #pragma unroll 8
                     for (int k = 0; k < 16; ++k) {
                         const uint32_t kk = c * 16 + k, blk = kk >> 2, sub = (kk & 3) * 32u;
                         umma_f16(d, sdesc_sw128(sb + Q_OFF + blk * 8192u + sub, 16, 1024),
-                                 sdesc_sw128(kv + blk * KV_BLOCK + sub, 16, 1024), id_s, k > 0);
+                                 sdesc_sw128(sb + kv_at(st, blk) + sub, 16, 1024), id, k > 0);
                     }
-                    umma_commit(bar(B_S_FULL + st));
-                    if (i == s.ntiles - 1 && next_reloads) umma_commit(bar(B_Q_EMPTY));
+                    for (int j = 0; j < nt; ++j) umma_commit(bar(B_S_FULL + st + j));
+                    i += nt;
+                    if (i == s.ntiles && next_reloads) umma_commit(bar(B_Q_EMPTY));
                 }
                 g += s.ntiles;
                 cur = nxt;
@@ -456,7 +537,7 @@ __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(const KParams 
         uint8_t *stage = base + EPI_OFF + static_cast<uint32_t>(wl) * 1024u;
         int g = 0, ks = 0;
         bool stop = false;
-        Unit cur = u_beg < u_end ? unit_info(kp, sp, u_beg) : Unit{};
+        Unit cur = first;
         for (int u = u_beg; u < u_end && !stop; ++u) {
             const Unit nxt = u + 1 < u_end ? unit_info(kp, sp, u + 1) : cur;
             const Unit &s = cur;
@@ -474,8 +555,8 @@ __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(const KParams 
                         uint32_t sa[NT / 2], sc[NT / 2];
 #pragma unroll
                         for (int hf = 0; hf < 2; ++hf) {        // the two reduction halves of S, 16 columns at a time
-                            tmem_ld16(tmem + lane_base + TM_S + st * 2 * NT + hf * 16, sa);
-                            tmem_ld16(tmem + lane_base + TM_S + st * 2 * NT + NT + hf * 16, sc);
+                            tmem_ld16(tmem + lane_base + TM_S + st * NT + hf * 16, sa);
+                            tmem_ld16(tmem + lane_base + TM_S + kStages * NT + st * NT + hf * 16, sc);
                             tmem_wait_ld();
 #pragma unroll
                             for (int j = 0; j < NT / 2; ++j)
@@ -573,13 +654,12 @@ __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(const KParams 
                     if (lane == 0) {
                         if (mbar_wait(bar(B_P_FULL + pb), (gi >> 1) & 1, abort_flag)) {
                             tc_fence_after();
-                            const uint32_t kv = sb + KV_OFF + st * KV_STAGE;
 #pragma unroll
                             for (int k = 0; k < 4; ++k) {
                                 const uint32_t half = k >> 1, sub = k & 1;
                                 const uint32_t a = sb + P_OFF + (half ? 0u : 8192u) + pb * 64u + sub * 32u;
-                                const uint32_t b = kv + half * 4u * KV_BLOCK + sub * 2048u;
-                                umma_f16(tmem + TM_O, sdesc_sw128(a, 16, 1024), sdesc_sw128(b, KV_BLOCK, 1024), id_pv,
+                                const uint32_t b = sb + kv_at(st, half * 4u) + sub * 2048u;
+                                umma_f16(tmem + TM_O, sdesc_sw128(a, 16, 1024), sdesc_sw128(b, KV_COL, 1024), id_pv,
                                          !(i == 0 && k == 0));
                             }
                             umma_commit(bar(B_KV_EMPTY + st));
@@ -615,52 +695,63 @@ __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(const KParams 
                 if (final_split && kp.sinks) den += exp2f(__ldg(kp.sinks + s.h0 + h) * 1.4426950408889634f - mm);
                 inv = 1.f / den;
             }
-            // O out of TMEM, normalised and packed to 16 bits (the output
-            // dtype for a final split, bf16 for a partial), in two halves of
-            // 128 columns; each half is written out through the warp's
-            // staging slice.  Coalesced stores: each lane parks 32 bytes of its
-            // row (16-byte pieces rotated by lane), then lane L writes piece
-            // L%2 of row 16k + L/2: one warp store covers sixteen 32-byte row
-            // segments (whole sectors).
+            // O out of TMEM (two 32-column chunks per wait), normalised and
+            // packed to 16 bits.
+            //  * a partial (bf16) goes to the workspace in chunk-major order
+            //    ([split][dim / 8][head][8]): for each 8-dim chunk the 32
+            //    lanes of a warp write 32 consecutive heads, 512 contiguous
+            //    bytes per warp store, straight from registers;
+            //  * a final split (output dtype) goes to the output rows through
+            //    the warp's staging slice: each lane parks 32 bytes of its row
+            //    (16-byte pieces rotated by lane), then lane L writes piece L%2
+            //    of row 16k + L/2 (sixteen 32-byte row segments per store).
             const bool out_bf16 = final_split ? bf16 : true;
-            uint16_t *obase = nullptr;
-            if (final_split) obase = static_cast<uint16_t *>(kp.out) + ((int64_t)s.t * kp.q_n + s.h0) * 512;
-            else if (ws_ok) obase = kp.ws_o + ((int64_t)s.w * kp.q_n + s.h0) * 512;
-            const int srow = lane >> 1, spiece = lane & 1;
             const int dcol = head_row ? 0 : 256;
+            const int hrow = (wl & 1) * 32 + lane;               // this lane's head within the group
+            uint16_t *obase = final_split ? static_cast<uint16_t *>(kp.out) + ((int64_t)s.t * kp.q_n + s.h0) * 512
+                                          : kp.ws_o + (int64_t)s.w * kp.q_n * 512;
+            const int srow = lane >> 1, spiece = lane & 1;
 #pragma unroll 1
-            for (int hf = 0; hf < 2; ++hf) {
-                uint32_t pk[64];
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t o[32];
-                    tmem_ld32(tmem + lane_base + TM_O + (hf * 4 + c) * 32, o);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int j = 0; j < 16; ++j)
-                        pk[c * 16 + j] = pack2(__uint_as_float(o[2 * j]) * inv, __uint_as_float(o[2 * j + 1]) * inv,
-                                               out_bf16);
-                }
-                // after the second half, TMEM is free for the next unit once
+            for (int cc = 0; cc < 8; cc += 2) {
+                uint32_t o[64];
+                tmem_ld32(tmem + lane_base + TM_O + cc * 32, *reinterpret_cast<uint32_t(*)[32]>(&o[0]));
+                tmem_ld32(tmem + lane_base + TM_O + cc * 32 + 32, *reinterpret_cast<uint32_t(*)[32]>(&o[32]));
+                tmem_wait_ld();
+                // after the last chunk, TMEM is free for the next unit once
                 // this warp's next P arrival (which follows this fence) completes
-                if (hf == 1) tc_fence_before();
-                if (!obase) continue;
+                if (cc == 6) tc_fence_before();
+                uint32_t pk[32];
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {                    // 16 columns per round
-                    __syncwarp();
+                for (int j = 0; j < 32; ++j)
+                    pk[j] = pack2(__uint_as_float(o[2 * j]) * inv, __uint_as_float(o[2 * j + 1]) * inv, out_bf16);
+                if (!final_split) {
+                    if (ws_ok && hrow < s.nh) {
 #pragma unroll
-                    for (int q = 0; q < 2; ++q)
-                        *reinterpret_cast<uint4 *>(stage + lane * 32 + ((q ^ (lane & 1)) << 4)) =
-                            make_uint4(pk[c * 8 + 4 * q], pk[c * 8 + 4 * q + 1], pk[c * 8 + 4 * q + 2],
-                                       pk[c * 8 + 4 * q + 3]);
-                    __syncwarp();
+                        for (int q = 0; q < 8; ++q) {            // 8-dim chunk (dcol + 32 cc) / 8 + q
+                            const int chunk = (dcol + cc * 32) / 8 + q;
+                            *reinterpret_cast<uint4 *>(obase + ((int64_t)chunk * kp.q_n + s.h0 + hrow) * 8) =
+                                make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+                        }
+                    }
+                } else {
 #pragma unroll
-                    for (int k = 0; k < 2; ++k) {
-                        const int lr = k * 16 + srow, hh = (wl & 1) * 32 + lr;
-                        const uint4 v = *reinterpret_cast<const uint4 *>(stage + lr * 32 + ((spiece ^ (lr & 1)) << 4));
-                        if (hh < s.nh)
-                            *reinterpret_cast<uint4 *>(obase + (int64_t)hh * 512 + dcol + hf * 128 + c * 16 +
-                                                       spiece * 8) = v;
+                    for (int r = 0; r < 4; ++r) {                // 16 columns per round
+                        __syncwarp();
+#pragma unroll
+                        for (int q = 0; q < 2; ++q)
+                            *reinterpret_cast<uint4 *>(stage + lane * 32 + ((q ^ (lane & 1)) << 4)) =
+                                make_uint4(pk[r * 8 + 4 * q], pk[r * 8 + 4 * q + 1], pk[r * 8 + 4 * q + 2],
+                                           pk[r * 8 + 4 * q + 3]);
+                        __syncwarp();
+#pragma unroll
+                        for (int k = 0; k < 2; ++k) {
+                            const int lr = k * 16 + srow, hh = (wl & 1) * 32 + lr;
+                            const uint4 v =
+                                *reinterpret_cast<const uint4 *>(stage + lr * 32 + ((spiece ^ (lr & 1)) << 4));
+                            if (hh < s.nh)
+                                *reinterpret_cast<uint4 *>(obase + (int64_t)hh * 512 + dcol + cc * 32 + r * 16 +
+                                                           spiece * 8) = v;
+                        }
                     }
                 }
             }

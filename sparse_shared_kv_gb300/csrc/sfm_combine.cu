@@ -80,11 +80,12 @@ __global__ void __launch_bounds__(kThreads) sfm_combine_kernel(KParams kp)
             const float wl = lane < cn ? expf(kp.ws_lse[(int64_t)(s0 + c + lane) * kp.q_n + h] - L) : 0.f;
             for (int s = 0; s < cn; ++s) {
                 const float w = __shfl_sync(0xffffffffu, wl, s);
-                const uint4 *src = reinterpret_cast<const uint4 *>(
-                    kp.ws_o + ((int64_t)(s0 + c + s) * kp.q_n + h) * 512 + lane * 16);
+                // chunk-major partial: [split][dim / 8][head][8]; this lane's
+                // 16 dims are chunks 2 lane and 2 lane + 1
+                const uint16_t *src = kp.ws_o + (int64_t)(s0 + c + s) * kp.q_n * 512;
 #pragma unroll
                 for (int q = 0; q < 2; ++q) {
-                    const uint4 v = src[q];
+                    const uint4 v = *reinterpret_cast<const uint4 *>(src + ((int64_t)(2 * lane + q) * kp.q_n + h) * 8);
                     const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {      // bf16 pair -> two floats (exact)

@@ -326,6 +326,7 @@ int sfm_metadata(const sfm_params *params, const sfm_tensors *lengths, int32_t *
     rc = validate_lengths(*params, lengths);
     if (rc) return rc;
     if (!metadata) return SFM_ERR_INVALID_ARG;
+    if ((uintptr_t)metadata & 15u) return SFM_ERR_LAYOUT;
     Plan pl;
     rc = make_plan(*params, &pl);
     if (rc) return rc;
@@ -348,6 +349,7 @@ int sfm_forward(const sfm_params *params, const sfm_tensors *in, const int32_t *
     rc = validate_tensors(p, in);
     if (rc) return rc;
     if (!out || !metadata || !isfinite(softmax_scale)) return SFM_ERR_INVALID_ARG;
+    if ((uintptr_t)metadata & 15u) return SFM_ERR_LAYOUT;
     if (!aligned16(out)) return SFM_ERR_LAYOUT;
     if (p.return_lse ? !lse : lse != nullptr) return SFM_ERR_INVALID_ARG;
     Plan pl;

@@ -24,6 +24,11 @@ namespace sfm {
 //   cp[T + 1]                 cost prefix per query row (attended rows + per-split overhead)
 //   rec[T][8]                 per query row: b, kv_len, cmp_len, p_cmp, lo, hi, n_ori, n_cmp
 //   own[Wcap]                 owning query row of every split
+//   srec[Wcap][16]            per split (64-byte aligned): t, first split of t, splits of t,
+//                             split size of t, then t's rec[8]; one 64-byte load gives a
+//                             kernel everything it needs about a split
+//   wrec[G][32]               per worker: first and end unit, 2 spare words, then the
+//                             srec of its first unit's split (one load to start work)
 // ----------------------------------------------------------------------------
 constexpr int32_t kMetaMagic = 0x53464d31;   // "SFM1"
 constexpr int kHdr = 16;
@@ -54,9 +59,19 @@ __host__ __device__ inline int64_t meta_split_off(int G) { return kHdr + (int64_
 __host__ __device__ inline int64_t meta_cost_off(int G, int T) { return kHdr + (int64_t)G + 1 + (int64_t)T + 1; }
 __host__ __device__ inline int64_t meta_rec_off(int G, int T) { return meta_cost_off(G, T) + (int64_t)T + 1; }
 __host__ __device__ inline int64_t meta_own_off(int G, int T) { return meta_rec_off(G, T) + (int64_t)kRecWords * T; }
+constexpr int kSrecWords = 16;
+constexpr int kWrecWords = 32;
+__host__ __device__ inline int64_t meta_srec_off(int G, int T, int64_t wcap)
+{
+    return (meta_own_off(G, T) + wcap + 15) & ~(int64_t)15;
+}
+__host__ __device__ inline int64_t meta_wrec_off(int G, int T, int64_t wcap)
+{
+    return meta_srec_off(G, T, wcap) + (int64_t)kSrecWords * wcap;
+}
 __host__ __device__ inline int64_t meta_words(int G, int T, int64_t wcap)
 {
-    int64_t n = meta_own_off(G, T) + wcap;
+    int64_t n = meta_wrec_off(G, T, wcap) + (int64_t)kWrecWords * G;
     return n < 1024 ? 1024 : n;
 }
 
@@ -93,7 +108,7 @@ struct KParams {
     int32_t *meta_w;
     void *out;
     float *lse;
-    uint16_t *ws_o;   // [capacity][q_n][512] normalised partial O, bf16
+    uint16_t *ws_o;   // [capacity][512 / 8][q_n][8] normalised partial O, bf16, chunk-major
     float *ws_lse;    // [capacity][q_n] partial LSE
     int32_t *status;
     int32_t *dbg_rows;

@@ -98,6 +98,8 @@ __global__ void __launch_bounds__(kPlanThreads) sfm_plan_kernel(KParams kp)
     int32_t *cp = meta + meta_cost_off(G, T);
     int32_t *rec = meta + meta_rec_off(G, T);
     int32_t *own = meta + meta_own_off(G, T);
+    int32_t *srec = meta + meta_srec_off(G, T, kp.wcap);
+    int32_t *wrec = meta + meta_wrec_off(G, T, kp.wcap);
     const bool in_smem = T <= kSmemRows;
     const int tid = threadIdx.x;
     if (tid == 0) {
@@ -143,7 +145,19 @@ __global__ void __launch_bounds__(kPlanThreads) sfm_plan_kernel(KParams kp)
             s_sp[t] = (int32_t)ex_s;
             s_cp[t] = (int32_t)ex_c;
         }
-        for (int64_t j = 0; j < ns && ex_s + j < kp.wcap; ++j) own[ex_s + j] = t;
+        if (ns > 0) {
+            const int32_t *r = rec + (int64_t)kRecWords * t;
+            int4 r0 = make_int4(r[0], r[1], r[2], r[3]), r1 = make_int4(r[4], r[5], r[6], r[7]);
+            const int4 hd = make_int4(t, (int32_t)ex_s, (int32_t)ns, split_size(n, S));
+            for (int64_t j = 0; j < ns && ex_s + j < kp.wcap; ++j) {
+                own[ex_s + j] = t;
+                int4 *d = reinterpret_cast<int4 *>(srec + (ex_s + j) * kSrecWords);
+                d[0] = hd;
+                d[1] = r0;
+                d[2] = r1;
+                d[3] = make_int4(0, 0, 0, 0);
+            }
+        }
         ex_s += ns;
         ex_c += n + ns * kSplitOverheadRows;
     }
@@ -198,6 +212,20 @@ __global__ void __launch_bounds__(kPlanThreads) sfm_plan_kernel(KParams kp)
         ws[c] = (int32_t)(u < INT32_MAX ? u : INT32_MAX);
     }
     __syncthreads();
+    // 4. per worker: its range and its first unit's split record in one place
+    for (int c = tid; c < G; c += kPlanThreads) {
+        const int32_t u0 = ws[c], u1 = ws[c + 1];
+        int4 *d = reinterpret_cast<int4 *>(wrec + (int64_t)c * kWrecWords);
+        d[0] = make_int4(u0, u1, 0, 0);
+        const int64_t w0 = u0 / HG;
+        if (u0 < u1 && w0 < kp.wcap) {
+            const int4 *src = reinterpret_cast<const int4 *>(srec + w0 * kSrecWords);
+            d[1] = src[0];
+            d[2] = src[1];
+            d[3] = src[2];
+            d[4] = src[3];
+        }
+    }
     if (tid == 0) {
         meta[H_MAGIC] = kMetaMagic;
         meta[H_FPRINT] = kp.fingerprint;

@@ -141,6 +141,33 @@ __device__ __forceinline__ void fence_proxy_async_smem()
 }
 
 // ---------------------------------------------------------------------------
+// L2 prefetch of a byte range (bulk, asynchronous; 16-byte aligned start,
+// size a multiple of 16)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+// Share c of G of a buffer of `bytes` bytes (at most `cap` bytes per share).
+__device__ __forceinline__ void prefetch_share(const void *base, int64_t bytes, int c, int G, int64_t cap)
+{
+    if (base == nullptr || bytes <= 0 || (reinterpret_cast<uintptr_t>(base) & 15u)) return;
+    int64_t per = ((bytes + G - 1) / G + 15) & ~static_cast<int64_t>(15);
+    if (per > cap) per = cap;
+    const int64_t off = per * c;
+    if (off >= bytes) return;
+    int64_t n = (bytes - off < per ? bytes - off : per) & ~static_cast<int64_t>(15);
+    const uint8_t *q = static_cast<const uint8_t *>(base) + off;
+    while (n > 0) {
+        const uint32_t chunk = n > 32768 ? 32768u : static_cast<uint32_t>(n);
+        prefetch_l2(q, chunk);
+        q += chunk;
+        n -= chunk;
+    }
+}
+
+// ---------------------------------------------------------------------------
 // per-warpgroup register budget (all four warps of a warpgroup execute it)
 // ---------------------------------------------------------------------------
 template <int N>
