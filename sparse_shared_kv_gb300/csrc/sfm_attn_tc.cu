@@ -68,22 +68,11 @@ namespace {
 using namespace tc;
 
 constexpr int NT = 32;                       // KV rows per tile
-constexpr int kStages = 4;                   // KV stages == S buffers
 constexpr int kThreads = 384;               // 12 warps: three warpgroups
 constexpr int kProducers = 4;               // KV copy warps
-constexpr uint32_t Q_OFF = 0;                // 8 blocks x 64 rows x 128 B
-constexpr uint32_t P_OFF = 65536;            // 192 rows x 128 B: [0..63] zero, [64..127] P, [128..191] zero
-constexpr uint32_t KV_OFF = 90112;           // 4 stages x 32 KB, column-block major (below)
 constexpr uint32_t KV_BLOCK = NT * 128;      // one 64-column block of one stage (32 rows)
-constexpr uint32_t KV_STAGE = 8 * KV_BLOCK;  // bytes of one stage
-constexpr uint32_t KV_COL = kStages * KV_BLOCK;   // stride between 64-column blocks
-// Column block a of stage st sits at KV_OFF + a * KV_COL + st * KV_BLOCK, so
-// stages 2j and 2j+1 form one contiguous 64-row operand per column block.
-__host__ __device__ constexpr uint32_t kv_at(uint32_t st, uint32_t a) { return KV_OFF + a * KV_COL + st * KV_BLOCK; }
-constexpr uint32_t MISC_OFF = KV_OFF + kStages * KV_STAGE;   // 221184
+constexpr uint32_t PK_ROW = 656;             // packed row: int8[512], rope bf16[64], fp32 scale[4]
 constexpr uint32_t MISC_BYTES = 4608;
-constexpr uint32_t EPI_OFF = MISC_OFF + MISC_BYTES;          // epilogue staging, 1 KB per softmax warp
-constexpr uint32_t kSmemBytes = EPI_OFF + 4 * 1024 + 1024;   // + alignment slack
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t TM_O = 0;                 // O: columns [0, 256)
 constexpr uint32_t TM_S = 256;               // S: chain c, stage s at [256 + 128 c + 32 s, +32)
@@ -91,8 +80,26 @@ constexpr float kRescaleThreshold = 8.0f;    // log2 units
 constexpr int kRing = 16;                    // resolved tiles in flight
 constexpr int kResolveBatch = 8;             // tiles per resolver batch
 
-static_assert(kSmemBytes <= 232448, "shared memory budget");
-static_assert(P_OFF == Q_OFF + 8 * 8192, "the last Q block's alias rows must be P's leading zero rows");
+// Shared-memory layout.  Plain rows: Q (8 column blocks of 64 values), P,
+// four 32-row bf16 stages.  Packed rows: Q and K carry 9 column blocks (512
+// dequantized values + 64 rope values), two bf16 stages and two raw stages
+// of 32 packed rows (the copy target the producers convert from).
+template <bool PK>
+struct Lay {
+    static constexpr int QB = PK ? 9 : 8;                        // 64-column blocks of a Q / K row
+    static constexpr int kStages = PK ? 2 : 4;                   // bf16 KV stages == S buffers
+    static constexpr uint32_t Q_OFF = 0;                         // QB blocks x 64 rows x 128 B
+    static constexpr uint32_t P_OFF = QB * 8192;                 // 192 rows x 128 B: zero / P / zero
+    static constexpr uint32_t KV_OFF = P_OFF + 24576;
+    static constexpr uint32_t KV_COL = kStages * KV_BLOCK;       // stride between 64-column blocks
+    static constexpr uint32_t RAW_OFF = KV_OFF + QB * KV_COL;
+    static constexpr uint32_t RAW_STAGE = NT * PK_ROW;
+    static constexpr uint32_t MISC_OFF = (RAW_OFF + (PK ? 2 * RAW_STAGE : 0) + 1023u) & ~1023u;
+    static constexpr uint32_t EPI_OFF = MISC_OFF + MISC_BYTES;   // epilogue staging, 1 KB per softmax warp
+    static constexpr uint32_t kSmemBytes = EPI_OFF + 4 * 1024 + 1024;   // + alignment slack
+    static_assert(kSmemBytes <= 232448, "shared memory budget");
+    static_assert(P_OFF == Q_OFF + QB * 8192, "the last Q block's alias rows must be P's leading zero rows");
+};
 
 // barrier slots (8 bytes each) at MISC_OFF
 enum Bar {
@@ -113,14 +120,15 @@ enum Bar {
     B_TEARDOWN_S2 = 61,
     kNumBars = 62
 };
-constexpr uint32_t TMEM_SLOT_OFF = MISC_OFF + 512;
-constexpr uint32_t ABORT_OFF = MISC_OFF + 516;
-constexpr uint32_t VALID_OFF = MISC_OFF + 528;   // [4] row-valid words
-constexpr uint32_t ALPHA_OFF = MISC_OFF + 1024;  // [4][64] floats
-constexpr uint32_t STATS_OFF = MISC_OFF + 2048;  // [64][2] floats
-constexpr uint32_t RING_OFF = MISC_OFF + 2560;   // [16][32] int32 row entries
+// offsets inside the misc area
+constexpr uint32_t TMEM_SLOT_REL = 512;
+constexpr uint32_t ABORT_REL = 516;
+constexpr uint32_t VALID_REL = 528;      // [4] row-valid words
+constexpr uint32_t ALPHA_REL = 1024;     // [4][64] floats
+constexpr uint32_t STATS_REL = 2048;     // [64][2] floats
+constexpr uint32_t RING_REL = 2560;      // [16][32] int32 row entries
 static_assert(kNumBars * 8 <= 512, "barrier area");
-static_assert(RING_OFF + kRing * NT * 4 <= MISC_OFF + MISC_BYTES, "misc area");
+static_assert(RING_REL + kRing * NT * 4 <= MISC_BYTES, "misc area");
 
 struct Unit {
     int t, w, h0, nh, nsplit, pos0, pos1, ntiles, key;
@@ -170,6 +178,31 @@ __device__ __forceinline__ Unit unit_info(const KParams &kp, const int32_t *srec
 {
     const int4 *r = reinterpret_cast<const int4 *>(srec + (int64_t)(u / kp.head_groups) * kSrecWords);
     return unit_decode(kp, __ldg(r), __ldg(r + 1), __ldg(r + 2), u);
+}
+
+// byte b of w as a signed 8-bit integer, converted exactly to float: the
+// sign-extended byte (prmt sign-replicate selector) added to the bit pattern
+// of 1.5 * 2^23, whose unit in the last place is 1, minus 1.5 * 2^23
+__device__ __forceinline__ float i8_to_f32(uint32_t w, int b)
+{
+    const uint32_t sel = (uint32_t)b | ((8u | b) << 4) | ((8u | b) << 8) | ((8u | b) << 12);
+    uint32_t v;
+    asm("prmt.b32 %0, %1, 0, %2;" : "=r"(v) : "r"(w), "r"(sel));
+    return __int_as_float(0x4B400000 + (int)v) - 12582912.0f;
+}
+
+// eight bf16 values -> eight fp16 values (round to nearest; exact for
+// magnitudes in fp16's normal range)
+__device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v)
+{
+    uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float a = __uint_as_float(w[i] << 16), b = __uint_as_float(w[i] & 0xffff0000u);
+        __half2 h = __floats2half2_rn(a, b);
+        w[i] = *reinterpret_cast<uint32_t *>(&h);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
 __device__ __forceinline__ uint32_t pack2(float a, float b, bool bf16)
@@ -265,8 +298,18 @@ __device__ __forceinline__ void resolve_tiles(const KParams &kp, const Unit &s, 
     if (err) set_status(kp, err);
 }
 
+template <bool PK>
 __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(const KParams kp)
 {
+    using L = Lay<PK>;
+    constexpr int QB = L::QB, kStages = L::kStages;
+    constexpr uint32_t Q_OFF = L::Q_OFF, P_OFF = L::P_OFF, KV_COL = L::KV_COL, MISC_OFF = L::MISC_OFF;
+    constexpr uint32_t EPI_OFF = L::EPI_OFF, TMEM_SLOT_OFF = MISC_OFF + TMEM_SLOT_REL, ABORT_OFF = MISC_OFF + ABORT_REL;
+    constexpr uint32_t VALID_OFF = MISC_OFF + VALID_REL, ALPHA_OFF = MISC_OFF + ALPHA_REL;
+    constexpr uint32_t STATS_OFF = MISC_OFF + STATS_REL, RING_OFF = MISC_OFF + RING_REL;
+    // Column block a of stage st sits at KV_OFF + a * KV_COL + st * KV_BLOCK, so
+    // stages 2j and 2j+1 form one contiguous 64-row operand per column block.
+    auto kv_at = [](uint32_t st, uint32_t a) -> uint32_t { return L::KV_OFF + a * KV_COL + st * KV_BLOCK; };
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t sb = smem_u32(base);
@@ -278,7 +321,12 @@ __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(const KParams 
     float *stats_s = reinterpret_cast<float *>(base + STATS_OFF);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const bool bf16 = kp.dtype == SFM_DTYPE_BF16;
+    const bool bf16 = kp.dtype == SFM_DTYPE_BF16;   // input / output dtype
+    // Operand dtype of the products.  Packed rows compute in fp16: int8 x
+    // scale rounded to fp16 (11-bit significand) keeps S within the LSE
+    // tolerance where bf16 (8-bit) does not; bf16 Q is converted exactly
+    // (magnitudes up to 65504).
+    const bool mma_bf16 = PK ? false : bf16;
     grid_launch_dependents();    // the combine kernel may launch; it waits for this grid
 
     // ---------------- set-up ----------------
@@ -286,12 +334,12 @@ __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(const KParams 
         reinterpret_cast<uint4 *>(base + P_OFF)[i] = make_uint4(0, 0, 0, 0);
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(bar(B_KV_FULL + s), 32 * kProducers + 1);
+            mbar_init(bar(B_KV_FULL + s), PK ? kProducers + 1 : 32 * kProducers + 1);
             mbar_init(bar(B_KV_EMPTY + s), 1);
             mbar_init(bar(B_S_FULL + s), 2);
             mbar_init(bar(B_S_FREE + s), 2);
-            mbar_init(bar(B_ALPHA + s), 2);
         }
+        for (int a = 0; a < 4; ++a) mbar_init(bar(B_ALPHA + a), 2);
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar(B_P_FULL + b), 4);
             mbar_init(bar(B_O_DONE + b), 1);
@@ -300,7 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(const KParams 
             mbar_init(bar(B_ROW_FULL + r), 1);
             mbar_init(bar(B_ROW_EMPTY + r), kProducers);
         }
-        mbar_init(bar(B_Q_FULL), 32 * kProducers);
+        mbar_init(bar(B_Q_FULL), (PK && kp.dtype == SFM_DTYPE_BF16) ? kProducers : 32 * kProducers);
         mbar_init(bar(B_Q_EMPTY), 2);
         mbar_init(bar(B_STATS), 2);
         mbar_init(bar(B_TEARDOWN), 1);
@@ -331,7 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(const KParams 
             prefetch_share(kp.ori_bt, (int64_t)kp.batch * kp.ori_bt_stride * 4, c, G, kCap);
             if (kp.has_cmp) prefetch_share(kp.cmp_bt, (int64_t)kp.batch * kp.cmp_bt_stride * 4, c, G, kCap);
         }
-        prefetch_share(kp.q, (int64_t)kp.T * kp.q_n * 1024, c, G, kCap);
+        prefetch_share(kp.q, (int64_t)kp.T * kp.q_n * QB * 128, c, G, kCap);
     }
 
     // everything above overlapped the planner; the plan is read from here on
@@ -396,21 +444,88 @@ __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(const KParams 
         // the unit's Q rows (16 heads per warp); rows past the group's heads are zero
         auto copy_q = [&](const Unit &s) -> bool {
             if (nq > 0 && !warp_wait(bar(B_Q_EMPTY), (nq - 1) & 1, abort_flag)) return false;
-            const uint8_t *qrow = static_cast<const uint8_t *>(kp.q) + ((int64_t)s.t * kp.q_n + s.h0) * 1024;
+            constexpr int QROW = QB * 128;                  // bytes of one Q head row
+            const uint8_t *qrow = static_cast<const uint8_t *>(kp.q) + ((int64_t)s.t * kp.q_n + s.h0) * QROW;
 #pragma unroll 4
             for (int rr = 0; rr < 64 / kProducers; ++rr) {
                 const int hh = pw * (64 / kProducers) + rr;
                 const bool live = hh < s.nh;
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    const int C = lane + half * 32;
-                    const uint32_t dst = sb + Q_OFF + (C >> 3) * 8192u + sw128(hh, C & 7);
-                    cp_async16(dst, live ? qrow + (int64_t)hh * 1024 + C * 16 : zero_src, live ? 16u : 0u);
+                for (int part = 0; part < (QB * 8 + 31) / 32; ++part) {
+                    const int C = lane + part * 32;
+                    if (C < QB * 8) {
+                        const uint32_t dst = sb + Q_OFF + (C >> 3) * 8192u + sw128(hh, C & 7);
+                        cp_async16(dst, live ? qrow + (int64_t)hh * QROW + C * 16 : zero_src, live ? 16u : 0u);
+                    }
                 }
             }
-            cp_async_arrive_noinc(bar(B_Q_FULL));
+            if (PK && bf16) {
+                // bf16 Q -> fp16 in place once this warp's rows have landed
+                cp_async_commit();
+                cp_async_wait<0>();
+                __syncwarp();
+                for (int rr = 0; rr < 64 / kProducers; ++rr) {
+                    const int hh = pw * (64 / kProducers) + rr;
+#pragma unroll
+                    for (int part = 0; part < (QB * 8 + 31) / 32; ++part) {
+                        const int C = lane + part * 32;
+                        if (C < QB * 8) {
+                            uint4 *q4 = reinterpret_cast<uint4 *>(base + Q_OFF + (C >> 3) * 8192u + sw128(hh, C & 7));
+                            *q4 = bf16x8_to_f16x8(*q4);
+                        }
+                    }
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(B_Q_FULL));
+            } else {
+                cp_async_arrive_noinc(bar(B_Q_FULL));
+            }
             ++nq;
             prev_key = s.key;
+            return true;
+        };
+        // packed rows: dequantize this warp's 8 rows of tile p from its raw
+        // stage into bf16 stage p % kStages (int8 x the row's per-128 fp32
+        // scale, rounded once; the 64 rope values are copied as they are)
+        int pend = -1;
+        uint32_t pend_vm = 0;
+        auto convert = [&](int p, uint32_t vmask, bool last) -> bool {
+            if (last) cp_async_wait<0>(); else cp_async_wait<1>();
+            __syncwarp();
+            const int st = p & (kStages - 1), use = p / kStages;
+            if (use >= 1 && !warp_wait(bar(B_KV_EMPTY + st), (use - 1) & 1, abort_flag)) return false;
+            const uint8_t *rawp = base + L::RAW_OFF + (p & 1) * L::RAW_STAGE;
+#pragma unroll 2
+            for (int k = 0; k < kRowsPerWarp; ++k) {
+                const int rr = pw * kRowsPerWarp + k;
+                const uint8_t *row = rawp + rr * PK_ROW;
+                const uint4 v = *reinterpret_cast<const uint4 *>(row + 16 * lane);   // dims 16 lane .. +15
+                const float sc = *reinterpret_cast<const float *>(row + 640 + 4 * (lane >> 3));
+                const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+                uint32_t o[8];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    o[2 * q] = pack2(i8_to_f32(w[q], 0) * sc, i8_to_f32(w[q], 1) * sc, false);
+                    o[2 * q + 1] = pack2(i8_to_f32(w[q], 2) * sc, i8_to_f32(w[q], 3) * sc, false);
+                }
+                const uint32_t dst = sb + kv_at(st, lane >> 2);
+                *reinterpret_cast<uint4 *>(base + (dst - sb) + sw128(rr, (lane & 3) * 2)) = make_uint4(o[0], o[1], o[2], o[3]);
+                *reinterpret_cast<uint4 *>(base + (dst - sb) + sw128(rr, (lane & 3) * 2 + 1)) =
+                    make_uint4(o[4], o[5], o[6], o[7]);
+                if (lane < 8) {                          // rope: input dtype -> fp16
+                    uint4 r4 = *reinterpret_cast<const uint4 *>(row + 512 + 16 * lane);
+                    if (bf16) r4 = bf16x8_to_f16x8(r4);
+                    *reinterpret_cast<uint4 *>(base + kv_at(st, 8) + sw128(rr, lane)) = r4;
+                }
+            }
+            fence_proxy_async_smem();      // generic-proxy writes -> tensor-core reads
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(B_KV_FULL + st));
+            if (pw == 0 && lane == 0) {
+                valid_s[st] = vmask;                     // the tile's row-valid bits
+                mbar_arrive(bar(B_KV_FULL + st));        // release: the word is visible with the phase
+            }
             return true;
         };
         Unit cur = first;
@@ -430,24 +545,43 @@ __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(const KParams 
                     row = e < 0 ? kp.cmp_kv + r * kp.cmp_row_stride : kp.ori_kv + r * kp.ori_row_stride;
                 }
                 const uint32_t vm = __ballot_sync(0xffffffffu, row != nullptr);
-                if (use >= 1 && !warp_wait(bar(B_KV_EMPTY + st), (use - 1) & 1, abort_flag)) { stop = true; break; }
-                const uint32_t stage = sb + kv_at(st, 0);
                 const unsigned long long my_row = reinterpret_cast<unsigned long long>(row);
+                if constexpr (!PK) {
+                    if (use >= 1 && !warp_wait(bar(B_KV_EMPTY + st), (use - 1) & 1, abort_flag)) { stop = true; break; }
+                    const uint32_t stage = sb + kv_at(st, 0);
 #pragma unroll
-                for (int k = 0; k < kRowsPerWarp; ++k) {
-                    const int rr = pw * kRowsPerWarp + k;
-                    const uint8_t *src = reinterpret_cast<const uint8_t *>(__shfl_sync(0xffffffffu, my_row, rr));
+                    for (int k = 0; k < kRowsPerWarp; ++k) {
+                        const int rr = pw * kRowsPerWarp + k;
+                        const uint8_t *src = reinterpret_cast<const uint8_t *>(__shfl_sync(0xffffffffu, my_row, rr));
 #pragma unroll
-                    for (int half = 0; half < 2; ++half) {
-                        const int C = lane + half * 32;
-                        const uint32_t dst = stage + (C >> 3) * KV_COL + sw128(rr, C & 7);
-                        cp_async16(dst, src ? src + C * 16 : zero_src, src ? 16u : 0u);
+                        for (int half = 0; half < 2; ++half) {
+                            const int C = lane + half * 32;
+                            const uint32_t dst = stage + (C >> 3) * KV_COL + sw128(rr, C & 7);
+                            cp_async16(dst, src ? src + C * 16 : zero_src, src ? 16u : 0u);
+                        }
                     }
-                }
-                cp_async_arrive_noinc(bar(B_KV_FULL + st));
-                if (pw == 0 && lane == 0) {
-                    valid_s[st] = vm;                        // the tile's row-valid bits
-                    mbar_arrive(bar(B_KV_FULL + st));        // release: the word is visible with the phase
+                    cp_async_arrive_noinc(bar(B_KV_FULL + st));
+                    if (pw == 0 && lane == 0) {
+                        valid_s[st] = vm;                        // the tile's row-valid bits
+                        mbar_arrive(bar(B_KV_FULL + st));        // release: the word is visible with the phase
+                    }
+                } else {
+                    // packed rows: 656 bytes each (41 x 16) into raw stage gi % 2,
+                    // then convert the tile copied one step earlier
+                    const uint32_t raw = sb + L::RAW_OFF + (gi & 1) * L::RAW_STAGE;
+#pragma unroll
+                    for (int k = 0; k < kRowsPerWarp; ++k) {
+                        const int rr = pw * kRowsPerWarp + k;
+                        const uint8_t *src = reinterpret_cast<const uint8_t *>(__shfl_sync(0xffffffffu, my_row, rr));
+                        const uint32_t dst = raw + rr * PK_ROW;
+                        cp_async16(dst + lane * 16, src ? src + lane * 16 : zero_src, src ? 16u : 0u);
+                        if (lane < PK_ROW / 16 - 32)
+                            cp_async16(dst + (32 + lane) * 16, src ? src + (32 + lane) * 16 : zero_src, src ? 16u : 0u);
+                    }
+                    cp_async_commit();
+                    if (pend >= 0 && !convert(pend, pend_vm, false)) { stop = true; break; }
+                    pend = gi;
+                    pend_vm = vm;
                 }
                 // Q after the unit's first tile: the first tile's row
                 // addresses are the longer dependency chain
@@ -455,6 +589,9 @@ __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(const KParams 
             }
             g += s.ntiles;
             cur = nxt;
+        }
+        if constexpr (PK) {
+            if (!stop && pend >= 0) convert(pend, pend_vm, true);
         }
         cp_async_wait<0>();
     } else if (warp == 8 || warp == 10) {
@@ -469,8 +606,8 @@ __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(const KParams 
         // bounds these small products).  P.V is issued by warp 6.
         if (lane == 0) {
             const int c = warp == 8 ? 0 : 1;
-            const uint32_t id_s = idesc_f16(128, NT, bf16, false, false);
-            const uint32_t id_s2 = idesc_f16(128, 2 * NT, bf16, false, false);
+            const uint32_t id_s = idesc_f16(128, NT, mma_bf16, false, false);
+            const uint32_t id_s2 = idesc_f16(128, 2 * NT, mma_bf16, false, false);
             int g = 0, nq = 0, prev_key = -1;
             bool stop = false;
             Unit cur = first;
@@ -501,8 +638,8 @@ __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(const KParams 
                     const uint32_t d = tmem + TM_S + c * (kStages * NT) + st * NT;
                     const uint32_t id = nt == 2 ? id_s2 : id_s;
 #pragma unroll 8
-                    for (int k = 0; k < 16; ++k) {
-                        const uint32_t kk = c * 16 + k, blk = kk >> 2, sub = (kk & 3) * 32u;
+                    for (int k = 0; k < 2 * QB; ++k) {
+                        const uint32_t kk = c * 2 * QB + k, blk = kk >> 2, sub = (kk & 3) * 32u;
                         umma_f16(d, sdesc_sw128(sb + Q_OFF + blk * 8192u + sub, 16, 1024),
                                  sdesc_sw128(sb + kv_at(st, blk) + sub, 16, 1024), id, k > 0);
                     }
@@ -533,7 +670,7 @@ __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(const KParams 
         const int wl = warp - 4;
         const uint32_t lane_base = static_cast<uint32_t>(wl * 32) << 16;
         const float sl2 = kp.scale_log2;
-        const uint32_t id_pv = idesc_f16(128, 256, bf16, false, true);
+        const uint32_t id_pv = idesc_f16(128, 256, mma_bf16, false, true);
         uint8_t *stage = base + EPI_OFF + static_cast<uint32_t>(wl) * 1024u;
         int g = 0, ks = 0;
         bool stop = false;
@@ -600,7 +737,7 @@ __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(const KParams 
                                 const float p0 = fast_exp2(fmaf(x[2 * j], sl2, nm));
                                 const float p1 = fast_exp2(fmaf(x[2 * j + 1], sl2, nm));
                                 ps[j] = p0 + p1;
-                                pw[j] = pack2(p0, p1, bf16);
+                                pw[j] = pack2(p0, p1, mma_bf16);
                             }
                         }
 #pragma unroll
@@ -609,12 +746,12 @@ __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(const KParams 
                             for (int j = 0; j < w2; ++j) ps[j] += ps[j + w2];
                         l = l * alpha + ps[0];
                     }
-                    alpha_s[st * 64 + r] = alpha;
+                    alpha_s[(gi & 3) * 64 + r] = alpha;      // four-slot ring, whatever the stage count
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(bar(B_ALPHA + st));
+                    if (lane == 0) mbar_arrive(bar(B_ALPHA + (gi & 3)));
                 } else {
-                    if (!warp_wait(bar(B_ALPHA + st), use & 1, abort_flag)) { stop = true; break; }
-                    alpha = alpha_s[st * 64 + h];
+                    if (!warp_wait(bar(B_ALPHA + (gi & 3)), (gi >> 2) & 1, abort_flag)) { stop = true; break; }
+                    alpha = alpha_s[(gi & 3) * 64 + h];
                 }
                 // rescale this warp's half of O once P.V(i-1) has landed in it
                 if (i > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
@@ -789,14 +926,20 @@ __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(const KParams 
     }
 }
 
+template <bool PK>
+cudaError_t launch_tc(const KParams &kp, cudaStream_t st)
+{
+    constexpr uint32_t smem = Lay<PK>::kSmemBytes;
+    cudaError_t e = cudaFuncSetAttribute(sfm_attn_tc_kernel<PK>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    return launch_dependent(sfm_attn_tc_kernel<PK>, dim3(kp.G), dim3(kThreads), (size_t)smem, st, kp);
+}
+
 }  // namespace
 
 cudaError_t launch_attn_tc(const KParams &kp, cudaStream_t st)
 {
-    cudaError_t e = cudaFuncSetAttribute(sfm_attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kSmemBytes);
-    if (e != cudaSuccess) return e;
-    return launch_dependent(sfm_attn_tc_kernel, dim3(kp.G), dim3(kThreads), kSmemBytes, st, kp);
+    return kp.packed ? launch_tc<true>(kp, st) : launch_tc<false>(kp, st);
 }
 
 }  // namespace sfm

@@ -293,9 +293,24 @@ def test_kernel_paths_prefill_fp16(hint):
 
 
 def test_tensor_core_hint_rejects_unsupported():
-    # quantized packed rows have no tensor-core path; asking for one is an error
+    # packed rows without the rope part (528 bytes) have no tensor-core path;
+    # asking for one is an error
     prob = S.build("packed_tc", seed=1, device="cuda", q_n=16, q_lens=[1], kv_lens=[300], layout_q="BSND",
                    layout_kv="PAGED", mode="ori_sparse", ori_topk=64, ori_mask_mode=3, cmp_mask_mode=0,
-                   kv_format="int8_packed", rope_head_dim=64, ori_block_size=64)
+                   kv_format="int8_packed", rope_head_dim=0, ori_block_size=64)
     with pytest.raises(sfm.SfmError):
         sfm.sfm_metadata_size(_sfm.params_of(prob, kernel_hint=2))
+
+
+@pytest.mark.parametrize("hint", [1, 2], ids=["cuda_core", "tensor_core"])
+@pytest.mark.parametrize("q_n", [16, 64, 128])
+def test_kernel_paths_packed(q_n, hint):
+    # packed int8 rows (656 bytes) with token-wise top-k over a paged pool;
+    # the index lists include masked (-1) and future entries
+    prob = S.build(f"packed{q_n}", seed=300 + q_n, device="cuda", q_n=q_n, q_lens=[1, 1, 1], kv_lens=[900, 3000, 200],
+                   layout_q="BSND", layout_kv="PAGED", mode="ori_sparse", ori_topk=256, ori_mask_mode=3,
+                   cmp_mask_mode=0, kv_format="int8_packed", rope_head_dim=64, ori_block_size=64,
+                   index_mode="any", softmax_scale=1.0 / 24.0)
+    out, lse, status = _sfm.Runner(prob, params=_sfm.params_of(prob, kernel_hint=hint)).run()
+    assert status in (0, 1), hex(status)       # out-of-range indices are flagged (BAD_INDEX) and skipped
+    assert_parity(prob, out, lse)
