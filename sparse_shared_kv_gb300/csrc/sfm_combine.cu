@@ -41,6 +41,7 @@ __global__ void __launch_bounds__(kThreads) sfm_combine_kernel(KParams kp)
 {
     const int t = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int h = blockIdx.y * kHeadsPerBlock + warp;
+    grid_launch_dependents();    // the next launch on the stream may start its set-up
     grid_dependency_wait();      // partial results come from the attention launch before this one
     const bool ok = meta_ok(kp);
     if (t == 0 && blockIdx.y == 0 && threadIdx.x == 0) {

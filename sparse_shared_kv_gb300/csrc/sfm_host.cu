@@ -9,7 +9,6 @@
 #include <math.h>
 #include <string.h>
 
-
 #include "sfm_internal.cuh"
 
 namespace sfm {
@@ -142,7 +141,10 @@ int make_plan(const sfm_params &p, Plan *pl)
     if (rc) return rc;
     if (p.kernel_hint == 2 && !tc_fits(p)) return SFM_ERR_UNSUPPORTED;
     pl->path = (p.kernel_hint == 1 || !tc_fits(p)) ? PATH_SIMT : PATH_TC;
-    pl->G = sms;
+    // The tensor-core kernel keeps one CTA per SM and leaves one SM to the
+    // planner kernel that runs just before it (the attention kernel's set-up
+    // overlaps the planner; a CTA placed on the planner's SM would start late).
+    pl->G = pl->path == PATH_TC && sms > 1 ? sms - 1 : sms;
     pl->T = num_tokens(p);
     const bool decode_like = p.max_seqlen_q <= 16;
     // Tensor-core tiles are 32 rows.  Up to 64 heads: splits of 5 tiles.  128
@@ -178,6 +180,11 @@ size_t ws_lse_offset(const sfm_params &p, int64_t cap)
 {
     size_t o = (size_t)cap * p.num_heads_q * 512 * sizeof(uint16_t);
     return (o + 255) & ~(size_t)255;
+}
+
+int head_groups(const sfm_params &p, const Plan &pl)
+{
+    return pl.path == PATH_TC ? (p.num_heads_q + 63) / 64 : 1;
 }
 
 size_t workspace_bytes_for(const sfm_params &p, const Plan &pl)
@@ -220,7 +227,7 @@ void fill_common(KParams &kp, const sfm_params &p, const Plan &pl)
     kp.split_rows = pl.split_rows;
     kp.path = pl.path;
     kp.fingerprint = (int32_t)fingerprint(p, pl);
-    kp.head_groups = pl.path == PATH_TC ? (p.num_heads_q + 63) / 64 : 1;
+    kp.head_groups = head_groups(p, pl);
     kp.wcap = pl.T * pl.max_splits_per_token;
 }
 

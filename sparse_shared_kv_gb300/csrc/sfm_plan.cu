@@ -24,7 +24,8 @@ namespace sfm {
 namespace {
 
 constexpr int kPlanThreads = 1024;
-constexpr int kSmemRows = 2048;          // rows whose prefixes are kept in shared memory
+constexpr int kSmemRows = 1024;          // rows whose records and prefixes stay in shared memory
+constexpr int kMaxWorkers = 256;
 
 // Exclusive prefix sums of two values per thread over the block: a shuffle
 // scan inside each warp, then one warp scans the 32 warp totals.
@@ -72,24 +73,25 @@ __device__ __forceinline__ void block_exclusive_scan2(int64_t &a, int64_t &b, in
     __syncthreads();
 }
 
-__device__ __forceinline__ int64_t row_positions(const int32_t *rec, int t)
-{
-    const int32_t *r = rec + (int64_t)kRecWords * t;
-    return (int64_t)r[6] + r[7];
-}
-
+// One CTA.  Rows up to kSmemRows keep their records and prefixes in shared
+// memory, so after the length loads of phase 1 every phase reads shared
+// memory only (no global write-then-read round trips).
 __global__ void __launch_bounds__(kPlanThreads) sfm_plan_kernel(KParams kp)
 {
-    __shared__ int64_t s_a[kPlanThreads];
-    __shared__ int64_t s_b[kPlanThreads];
-    __shared__ int32_t s_n[kSmemRows];
+    __shared__ int64_t s_a[32];
+    __shared__ int64_t s_b[32];
+    __shared__ int4 s_rec[kSmemRows][2];
     __shared__ int32_t s_sp[kSmemRows + 1];
     __shared__ int32_t s_cp[kSmemRows + 1];
+    __shared__ int32_t s_ws[kMaxWorkers + 1];
     __shared__ int s_overflow;
 
     // the attention kernel may start its set-up now; it waits for this grid
-    // to finish before it reads the plan
+    // to finish before it reads the plan.  This grid itself is launched as a
+    // dependent of whatever ran before it on the stream (its launch latency
+    // overlaps that kernel's tail) and waits for it before reading any input.
     grid_launch_dependents();
+    grid_dependency_wait();
 
     int32_t *meta = kp.meta_w;
     const int T = kp.T, G = kp.G, S = kp.split_rows;
@@ -101,6 +103,7 @@ __global__ void __launch_bounds__(kPlanThreads) sfm_plan_kernel(KParams kp)
     int32_t *srec = meta + meta_srec_off(G, T, kp.wcap);
     int32_t *wrec = meta + meta_wrec_off(G, T, kp.wcap);
     const bool in_smem = T <= kSmemRows;
+    const bool ws_smem = G <= kMaxWorkers;
     const int tid = threadIdx.x;
     if (tid == 0) {
         s_overflow = 0;
@@ -109,25 +112,40 @@ __global__ void __launch_bounds__(kPlanThreads) sfm_plan_kernel(KParams kp)
     __syncthreads();
     kp.status = meta + H_LENFLAGS;
 
-    // 1. every row once: its record (and its position count)
+    auto rec_of = [&](int t, int4 &r0, int4 &r1) {
+        if (in_smem) {
+            r0 = s_rec[t][0];
+            r1 = s_rec[t][1];
+        } else {
+            const int32_t *r = rec + (int64_t)kRecWords * t;
+            r0 = make_int4(r[0], r[1], r[2], r[3]);
+            r1 = make_int4(r[4], r[5], r[6], r[7]);
+        }
+    };
+    auto count = [&](int t) -> int64_t {
+        int4 r0, r1;
+        rec_of(t, r0, r1);
+        return (int64_t)r1.z + r1.w;     // n_ori + n_cmp
+    };
+
+    // 1. every row once: lengths, window and position counts
     for (int t = tid; t < T; t += kPlanThreads) {
         const Tok k = token_info(kp, t);
-        int32_t *r = rec + (int64_t)kRecWords * t;
-        r[0] = k.b;
-        r[1] = k.kv_len;
-        r[2] = k.cmp_len;
-        r[3] = k.p_cmp;
-        r[4] = k.lo;
-        r[5] = k.hi;
-        r[6] = k.n_ori;
-        r[7] = k.n_cmp;
-        if (in_smem) s_n[t] = k.n_ori + k.n_cmp;
+        const int4 r0 = make_int4(k.b, k.kv_len, k.cmp_len, k.p_cmp), r1 = make_int4(k.lo, k.hi, k.n_ori, k.n_cmp);
+        if (in_smem) {
+            s_rec[t][0] = r0;
+            s_rec[t][1] = r1;
+        } else {
+            int32_t *r = rec + (int64_t)kRecWords * t;
+            r[0] = r0.x; r[1] = r0.y; r[2] = r0.z; r[3] = r0.w;
+            r[4] = r1.x; r[5] = r1.y; r[6] = r1.z; r[7] = r1.w;
+        }
     }
     __syncthreads();
-    // 2. split / cost prefixes: each thread scans a contiguous run of rows
+    // 2. split / cost prefixes: each thread scans a contiguous run of rows and
+    //    writes the split records of its rows
     const int per = (T + kPlanThreads - 1) / kPlanThreads;
     const int beg = min(T, tid * per), end = min(T, beg + per);
-    auto count = [&](int t) -> int64_t { return in_smem ? (int64_t)s_n[t] : row_positions(rec, t); };
     int64_t sum_s = 0, sum_c = 0;
     for (int t = beg; t < end; ++t) {
         const int64_t n = count(t), ns = n > 0 ? (n + S - 1) / S : 0;
@@ -146,8 +164,8 @@ __global__ void __launch_bounds__(kPlanThreads) sfm_plan_kernel(KParams kp)
             s_cp[t] = (int32_t)ex_c;
         }
         if (ns > 0) {
-            const int32_t *r = rec + (int64_t)kRecWords * t;
-            int4 r0 = make_int4(r[0], r[1], r[2], r[3]), r1 = make_int4(r[4], r[5], r[6], r[7]);
+            int4 r0, r1;
+            rec_of(t, r0, r1);
             const int4 hd = make_int4(t, (int32_t)ex_s, (int32_t)ns, split_size(n, S));
             for (int64_t j = 0; j < ns && ex_s + j < kp.wcap; ++j) {
                 own[ex_s + j] = t;
@@ -202,28 +220,44 @@ __global__ void __launch_bounds__(kPlanThreads) sfm_plan_kernel(KParams kp)
             } else {
                 const int64_t nu = (int64_t)(xsp[lo + 1] - xsp[lo]) * HG;
                 const int64_t within = target - (int64_t)xcp[lo] * HG;
-                const int64_t ucost = split_size(in_smem ? (int64_t)s_n[lo] : row_positions(rec, lo), S) +
-                                      kSplitOverheadRows;
+                const int64_t ucost = split_size(count(lo), S) + kSplitOverheadRows;
                 int64_t k = (within + ucost - 1) / ucost;
                 if (k > nu) k = nu;
                 u = (int64_t)xsp[lo] * HG + k;
             }
         }
-        ws[c] = (int32_t)(u < INT32_MAX ? u : INT32_MAX);
+        const int32_t v = (int32_t)(u < INT32_MAX ? u : INT32_MAX);
+        ws[c] = v;
+        if (ws_smem) s_ws[c] = v;
     }
     __syncthreads();
     // 4. per worker: its range and its first unit's split record in one place
     for (int c = tid; c < G; c += kPlanThreads) {
-        const int32_t u0 = ws[c], u1 = ws[c + 1];
+        const int32_t u0 = ws_smem ? s_ws[c] : ws[c], u1 = ws_smem ? s_ws[c + 1] : ws[c + 1];
         int4 *d = reinterpret_cast<int4 *>(wrec + (int64_t)c * kWrecWords);
         d[0] = make_int4(u0, u1, 0, 0);
         const int64_t w0 = u0 / HG;
         if (u0 < u1 && w0 < kp.wcap) {
-            const int4 *src = reinterpret_cast<const int4 *>(srec + w0 * kSrecWords);
-            d[1] = src[0];
-            d[2] = src[1];
-            d[3] = src[2];
-            d[4] = src[3];
+            if (in_smem) {
+                int lo = 0, hi = T - 1;          // the row owning split w0
+                while (lo < hi) {
+                    int mid = (lo + hi + 1) >> 1;
+                    if (s_sp[mid] <= w0) lo = mid; else hi = mid - 1;
+                }
+                const int64_t n = count(lo), ns = s_sp[lo + 1] - s_sp[lo];
+                int4 r0, r1;
+                rec_of(lo, r0, r1);
+                d[1] = make_int4(lo, s_sp[lo], (int32_t)ns, split_size(n, S));
+                d[2] = r0;
+                d[3] = r1;
+                d[4] = make_int4(0, 0, 0, 0);
+            } else {
+                const int4 *src = reinterpret_cast<const int4 *>(srec + w0 * kSrecWords);
+                d[1] = src[0];
+                d[2] = src[1];
+                d[3] = src[2];
+                d[4] = src[3];
+            }
         }
     }
     if (tid == 0) {
@@ -244,8 +278,7 @@ __global__ void __launch_bounds__(kPlanThreads) sfm_plan_kernel(KParams kp)
 
 cudaError_t launch_plan(const KParams &kp, cudaStream_t st)
 {
-    sfm_plan_kernel<<<1, kPlanThreads, 0, st>>>(kp);
-    return cudaGetLastError();
+    return launch_dependent(sfm_plan_kernel, dim3(1), dim3(kPlanThreads), (size_t)0, st, kp);
 }
 
 }  // namespace sfm
