@@ -134,7 +134,10 @@ typedef struct sfm_params {
     int32_t cmp_block_size;    /* paged with cmp_kv: rows per cmp block, multiple of 16, <= 1024 */
     int32_t return_lse;        /* 1: write LSE (fp32, token-major x q_n) */
     int32_t kernel_hint;       /* 0: automatic; 1: CUDA-core kernel; 2: tensor-core kernel
-                                  (SFM_ERR_UNSUPPORTED when the params do not fit it) */
+                                  (SFM_ERR_UNSUPPORTED when the params do not fit it: it
+                                  takes up to 128 heads with plain rows, or packed rows
+                                  with a 64-value rope part; packed rows are computed
+                                  with fp16 operands, bf16 q converted exactly) */
 } sfm_params;
 
 /* Device tensors of one call.  Shapes (row = one KV row of row_stride bytes):
