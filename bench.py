@@ -181,6 +181,13 @@ def accounting(prob, sfm):
     torch.cuda.synchronize()
     valid = rows >= 0
     attended = int(valid.sum().item())
+    # distinct KV rows read by the batch: (batch, source, logical row) triples;
+    # query rows of one sequence share most of their rows in prefill
+    qlens = torch.tensor(list(prob.q_lens) if prob.layout_q == "TND" else [prob.max_seqlen_q] * prob.batch_size,
+                         dtype=torch.int64, device=dev)
+    tok_b = torch.repeat_interleave(torch.arange(prob.batch_size, device=dev), qlens)[:prob.num_tokens]
+    keys = (tok_b[:, None] << 32) | rows.to(torch.int64)
+    distinct = int(torch.unique(keys[valid]).numel())
     # block-table entries touched: distinct (row, source, block) per query row
     bt_entries = 0
     if prob.layout_kv == "PAGED":
@@ -197,10 +204,11 @@ def accounting(prob, sfm):
     T, qn = prob.num_tokens, prob.num_heads_q
     row_bytes = prob.kv_row_bytes()
     idx_entries = T * (prob.ori_topk + prob.cmp_topk)
-    bytes_ = (attended * row_bytes + T * qn * prob.d_qk * 2 + T * qn * 512 * 2 + T * qn * 4 + idx_entries * 4
+    bytes_ = (distinct * row_bytes + T * qn * prob.d_qk * 2 + T * qn * 512 * 2 + T * qn * 4 + idx_entries * 4
               + bt_entries * 4 + prob.batch_size * 4 * 3)
     flops = attended * qn * (2 * prob.d_qk + 2 * 512)
-    return {"attended_rows": attended, "bytes": bytes_, "flops": flops, "bt_entries": bt_entries}
+    return {"attended_rows": attended, "distinct_rows": distinct, "bytes": bytes_, "flops": flops,
+            "bt_entries": bt_entries}
 
 
 def kernel_source_hash():
