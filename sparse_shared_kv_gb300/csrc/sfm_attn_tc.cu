@@ -303,6 +303,11 @@ __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(const KParams 
 {
     using L = Lay<PK>;
     constexpr int QB = L::QB, kStages = L::kStages;
+    // independent accumulation chains of S (TMEM: chain c, stage s at
+    // TM_S + 32 (c * kStages + s)); packed rows have two stages, which leaves
+    // room for four shorter chains
+    constexpr int kChains = PK ? 4 : 2;
+    static_assert(kChains * kStages * NT <= 256, "S buffers fit next to O in TMEM");
     constexpr uint32_t Q_OFF = L::Q_OFF, P_OFF = L::P_OFF, KV_COL = L::KV_COL, MISC_OFF = L::MISC_OFF;
     constexpr uint32_t EPI_OFF = L::EPI_OFF, TMEM_SLOT_OFF = MISC_OFF + TMEM_SLOT_REL, ABORT_OFF = MISC_OFF + ABORT_REL;
     constexpr uint32_t VALID_OFF = MISC_OFF + VALID_REL, ALPHA_OFF = MISC_OFF + ALPHA_REL;
@@ -624,7 +629,9 @@ __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(const KParams 
                     const int gi = g + i, st = gi & (kStages - 1), use = gi / kStages;
                     // an even tile and the next one of the same unit share one
                     // 64-row S (stages 2j, 2j+1 are one operand)
-                    const int nt = ((gi & 1) == 0 && i + 1 < s.ntiles) ? 2 : 1;
+                    // (packed rows have two stages only: a pair would hold both
+                    // and stop the conversion of the next tile from overlapping)
+                    const int nt = (!PK && (gi & 1) == 0 && i + 1 < s.ntiles) ? 2 : 1;
                     bool good = true;
                     for (int j = 0; j < nt && good; ++j)
                         good = mbar_wait(bar(B_KV_FULL + st + j), use & 1, abort_flag) &&
@@ -635,13 +642,20 @@ __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(const KParams 
                     }
                     fence_proxy_async_smem();    // cp.async (generic proxy) writes -> tensor-core reads
                     tc_fence_after();
-                    const uint32_t d = tmem + TM_S + c * (kStages * NT) + st * NT;
                     const uint32_t id = nt == 2 ? id_s2 : id_s;
-#pragma unroll 8
-                    for (int k = 0; k < 2 * QB; ++k) {
-                        const uint32_t kk = c * 2 * QB + k, blk = kk >> 2, sub = (kk & 3) * 32u;
-                        umma_f16(d, sdesc_sw128(sb + Q_OFF + blk * 8192u + sub, 16, 1024),
-                                 sdesc_sw128(sb + kv_at(st, blk) + sub, 16, 1024), id, k > 0);
+                    // this warp's kChains / 2 chains, interleaved step by step;
+                    // chain cc covers reduction steps [cc * kSteps, (cc + 1) * kSteps)
+                    constexpr int kSteps = QB * 4 / kChains;
+#pragma unroll 3
+                    for (int k = 0; k < kSteps; ++k) {
+#pragma unroll
+                        for (int j = 0; j < kChains / 2; ++j) {
+                            const int cc = c * (kChains / 2) + j;
+                            const uint32_t d = tmem + TM_S + cc * (kStages * NT) + st * NT;
+                            const uint32_t kk = cc * kSteps + k, blk = kk >> 2, sub = (kk & 3) * 32u;
+                            umma_f16(d, sdesc_sw128(sb + Q_OFF + blk * 8192u + sub, 16, 1024),
+                                     sdesc_sw128(sb + kv_at(st, blk) + sub, 16, 1024), id, k > 0);
+                        }
                     }
                     for (int j = 0; j < nt; ++j) umma_commit(bar(B_S_FULL + st + j));
                     i += nt;
@@ -691,13 +705,23 @@ __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(const KParams 
                     {
                         uint32_t sa[NT / 2], sc[NT / 2];
 #pragma unroll
-                        for (int hf = 0; hf < 2; ++hf) {        // the two reduction halves of S, 16 columns at a time
+                        for (int hf = 0; hf < 2; ++hf) {        // the chains' partial sums of S, 16 columns at a time
                             tmem_ld16(tmem + lane_base + TM_S + st * NT + hf * 16, sa);
                             tmem_ld16(tmem + lane_base + TM_S + kStages * NT + st * NT + hf * 16, sc);
                             tmem_wait_ld();
 #pragma unroll
                             for (int j = 0; j < NT / 2; ++j)
                                 sv[hf * 16 + j] = __float_as_uint(__uint_as_float(sa[j]) + __uint_as_float(sc[j]));
+#pragma unroll
+                            for (int cc = 2; cc < kChains; cc += 2) {
+                                tmem_ld16(tmem + lane_base + TM_S + cc * kStages * NT + st * NT + hf * 16, sa);
+                                tmem_ld16(tmem + lane_base + TM_S + (cc + 1) * kStages * NT + st * NT + hf * 16, sc);
+                                tmem_wait_ld();
+#pragma unroll
+                                for (int j = 0; j < NT / 2; ++j)
+                                    sv[hf * 16 + j] = __float_as_uint(__uint_as_float(sv[hf * 16 + j]) +
+                                                                      (__uint_as_float(sa[j]) + __uint_as_float(sc[j])));
+                            }
                         }
                     }
                     tc_fence_before();
