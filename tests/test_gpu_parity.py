@@ -255,6 +255,63 @@ def test_public_two_call_api():
     assert_parity(prob, out, lse)
 
 
+def _api_call(prob, T, out, lse, stream):
+    md = sfm.sparse_flash_mla_metadata(
+        prob.num_heads_q, 1, 512, seqused_ori_kv=T["seqused_ori_kv"], seqused_cmp_kv=T["seqused_cmp_kv"],
+        cmp_residual_kv=T["cmp_residual_kv"], batch_size=prob.batch_size, max_seqlen_q=1,
+        max_seqlen_ori_kv=prob.max_seqlen_ori_kv, max_seqlen_cmp_kv=prob.max_seqlen_cmp_kv,
+        cmp_topk=prob.cmp_topk, cmp_ratio=prob.cmp_ratio, ori_mask_mode=prob.ori_mask_mode,
+        cmp_mask_mode=prob.cmp_mask_mode, ori_win_left=prob.ori_win_left, ori_win_right=prob.ori_win_right,
+        layout_q="BSND", layout_kv="PAGED", ori_block_size=prob.ori_block_size,
+        cmp_block_size=prob.cmp_block_size, return_softmax_lse=True, stream=stream)
+    sfm.sparse_flash_mla(
+        T["q"], metadata=md, ori_kv=T["ori_kv"], cmp_kv=T["cmp_kv"], cmp_sparse_indices=T["cmp_sparse_indices"],
+        ori_block_table=T["ori_block_table"], cmp_block_table=T["cmp_block_table"],
+        seqused_ori_kv=T["seqused_ori_kv"], seqused_cmp_kv=T["seqused_cmp_kv"],
+        cmp_residual_kv=T["cmp_residual_kv"], sinks=T["sinks"], softmax_scale=prob.softmax_scale, out=out,
+        lse=lse, stream=stream)
+
+
+def test_two_call_api_in_cuda_graphs_on_two_streams():
+    """Both calls captured in a CUDA graph (planner, attention and combine
+    chained by programmatic dependent launch), two independent problems
+    replayed alternately on two streams: results equal the eager calls bit
+    for bit and meet the oracle."""
+    probs = [S.csa_decode(device="cuda", batch=5, seed=71), S.csa_decode(device="cuda", batch=7, seed=72)]
+    eager, graphs, outs = [], [], []
+    for prob in probs:
+        T = prob.t
+        out = torch.empty(T["q"].shape, dtype=T["q"].dtype, device="cuda")
+        lse = torch.empty(prob.num_tokens * prob.num_heads_q, dtype=torch.float32, device="cuda")
+        _api_call(prob, T, out, lse, torch.cuda.current_stream())
+        torch.cuda.synchronize()
+        eager.append((out.clone(), lse.clone()))
+        out.zero_()
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            _api_call(prob, T, out, lse, side)
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            _api_call(prob, T, out, lse, torch.cuda.current_stream())
+        graphs.append(g)
+        outs.append((out, lse))
+    for o, l in outs:
+        o.zero_()
+        l.zero_()
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    for k in range(8):
+        with torch.cuda.stream(streams[k % 2]):
+            graphs[k % 2].replay()
+    torch.cuda.synchronize()
+    for prob, (o, l), (eo, el) in zip(probs, outs, eager):
+        assert torch.equal(o, eo) and torch.equal(l, el)
+        assert_parity(prob, o, l)
+
+
 # ---------------------------------------------------------------------------
 # both attention kernels on the shapes the tensor-core kernel covers
 # ---------------------------------------------------------------------------
