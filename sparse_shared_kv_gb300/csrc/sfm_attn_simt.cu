@@ -153,7 +153,8 @@ __global__ void __launch_bounds__(kThreads) sfm_attn_simt_kernel(KParams kp)
         const int pos0 = sidx * size;
         const int pos1 = min(n, pos0 + size);
         const bool final_split = nsplit == 1;
-        if (!final_split && w >= kp.ws_capacity_splits) {
+        const int64_t slot = (int64_t)t * kp.max_splits + sidx;     // the row's workspace slot for this split
+        if (!final_split && (kp.max_splits <= 1 || sidx >= kp.max_splits)) {
             set_status(kp, SFM_STATUS_WORKSPACE_OVERFLOW);
             continue;
         }
@@ -258,11 +259,11 @@ __global__ void __launch_bounds__(kThreads) sfm_attn_simt_kernel(KParams kp)
             } else {
                 const float inv = l > 0.f ? 1.f / l : 0.f;
                 // chunk-major partial: [split][dim / 8][head][8]
-                uint16_t *o = kp.ws_o + (int64_t)w * kp.q_n * 512;
+                uint16_t *o = kp.ws_o + slot * kp.q_n * 512;
                 const int d0 = tid, d1 = tid + 256;
                 o[((int64_t)(d0 >> 3) * kp.q_n + hh) * 8 + (d0 & 7)] = float_to_half(acc[h][0] * inv, SFM_DTYPE_BF16);
                 o[((int64_t)(d1 >> 3) * kp.q_n + hh) * 8 + (d1 & 7)] = float_to_half(acc[h][1] * inv, SFM_DTYPE_BF16);
-                if (tid == 0) kp.ws_lse[(int64_t)w * kp.q_n + hh] = l > 0.f ? m + logf(l) : -INFINITY;
+                if (tid == 0) kp.ws_lse[slot * kp.q_n + hh] = l > 0.f ? m + logf(l) : -INFINITY;
             }
         }
     }

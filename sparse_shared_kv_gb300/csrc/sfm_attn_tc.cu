@@ -79,6 +79,8 @@ constexpr uint32_t TM_S = 256;               // S: chain c, stage s at [256 + 12
 constexpr float kRescaleThreshold = 8.0f;    // log2 units
 constexpr int kRing = 16;                    // resolved tiles in flight
 constexpr int kResolveBatch = 8;             // tiles per resolver batch
+constexpr int kFirstBatch = 4;               // tiles of a worker's first resolver batch
+constexpr int kPrefetchTiles = 4;            // tiles past the stages whose rows are prefetched to L2
 
 // Shared-memory layout.  Plain rows: Q (8 column blocks of 64 values), P,
 // four 32-row bf16 stages.  Packed rows: Q and K carry 9 column blocks (512
@@ -147,9 +149,11 @@ __device__ __forceinline__ Unit unit_decode(const KParams &kp, int4 r0, int4 r1,
     s.nsplit = r0.z;
     const int size = r0.w;
     const int local = u - s_beg * HG;
-    const int hg = s.nsplit > 0 ? local / s.nsplit : 0;
+    // head group of the unit: units of a row are group-major, at most two
+    // groups (128 heads)
+    const int hg = (HG > 1 && s.nsplit > 0 && local >= s.nsplit) ? 1 : 0;
     const int sidx = local - hg * s.nsplit;
-    s.w = s_beg + sidx;
+    s.w = sidx;          // the row's workspace slot t * max_splits + sidx holds its partial
     s.h0 = hg * 64;
     s.nh = min(64, kp.q_n - s.h0);
     s.key = s.t * HG + hg;
@@ -259,14 +263,15 @@ __device__ __forceinline__ void resolve_tiles(const KParams &kp, const Unit &s, 
     // 2. logical rows -> pool rows
     int64_t row[K];
     if (kp.layout_kv == SFM_LAYOUT_PAGED) {
-        int32_t blk[K];
+        int32_t blk[K], off[K];
         bool inb[K];
 #pragma unroll
         for (int j = 0; j < K; ++j) {
             const int bs = cmp[j] ? kp.cmp_bs : kp.ori_bs;
             const int bts = cmp[j] ? kp.cmp_bt_stride : kp.ori_bt_stride;
             const int ee = in[j] ? e[j] : 0;
-            const int bi = ee / bs;
+            const int bi = (int)fdiv((uint32_t)ee, cmp[j] ? kp.cmp_bs_div : kp.ori_bs_div);
+            off[j] = ee - bi * bs;
             inb[j] = in[j] && bi < bts;
             const int32_t *bp = inb[j] ? (cmp[j] ? kp.cmp_bt : kp.ori_bt) + (int64_t)k.b * bts + bi : safe;
             blk[j] = __ldg(bp);
@@ -274,7 +279,7 @@ __device__ __forceinline__ void resolve_tiles(const KParams &kp, const Unit &s, 
 #pragma unroll
         for (int j = 0; j < K; ++j) {
             const int bs = cmp[j] ? kp.cmp_bs : kp.ori_bs;
-            row[j] = (inb[j] && blk[j] >= 0) ? (int64_t)blk[j] * bs + (in[j] ? e[j] : 0) % bs : -1;
+            row[j] = (inb[j] && blk[j] >= 0) ? (int64_t)blk[j] * bs + off[j] : -1;
         }
     } else if (kp.layout_kv == SFM_LAYOUT_TND) {
         const int64_t base_o = __ldg(kp.cu_ori + k.b);
@@ -413,22 +418,48 @@ __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(const KParams 
         for (int u = u_beg; u < u_end && !stop; ++u) {
             const Unit nxt = u + 1 < u_end ? unit_info(kp, sp, u + 1) : cur;   // prefetched
             const Unit &s = cur;
-            for (int i0 = 0; i0 < s.ntiles && !stop; i0 += kResolveBatch) {
-                int32_t ent[kResolveBatch];
-                resolve_tiles<kResolveBatch>(kp, s, i0, lane, ent);
-#pragma unroll
-                for (int j = 0; j < kResolveBatch; ++j) {
+            // publish tiles i0 .. i0 + K - 1 of the unit, then pull the rows
+            // of the worker's tiles kStages .. kStages + kPrefetchTiles - 1
+            // into L2: those tiles wait for a stage to drain before their
+            // copies start, and then hit L2
+            auto publish = [&](int i0, int K, const int32_t *ent) {
+                for (int j = 0; j < K; ++j) {
                     const int i = i0 + j;
                     if (i >= s.ntiles) break;
                     const int gi = g + i, slot = gi % kRing, use = gi / kRing;
                     if (use >= 1 && !warp_wait(bar(B_ROW_EMPTY + slot), (use - 1) & 1, abort_flag)) {
                         stop = true;
-                        break;
+                        return;
                     }
                     ring[slot * NT + lane] = ent[j];
                     __syncwarp();
                     if (lane == 0) mbar_arrive(bar(B_ROW_FULL + slot));
                 }
+                for (int j = 0; j < K; ++j) {
+                    const int gi = g + i0 + j;
+                    if (i0 + j < s.ntiles && gi >= kStages && gi < kStages + kPrefetchTiles && ent[j] != -1) {
+                        const int64_t r = ent[j] & 0x7fffffff;
+                        const uint8_t *row = ent[j] < 0 ? kp.cmp_kv + r * kp.cmp_row_stride : kp.ori_kv + r * kp.ori_row_stride;
+                        constexpr uint32_t kRowBytes = PK ? PK_ROW : QB * 128u;
+#pragma unroll
+                        for (uint32_t o = 0; o < kRowBytes; o += 128) prefetch_line_l2(row + o);
+                        prefetch_line_l2(row + kRowBytes - 1);
+                    }
+                }
+            };
+            int i0 = 0;
+            if (g == 0 && s.ntiles > 0) {
+                // the worker's first tiles: a short batch (fewer instructions
+                // before the first publish)
+                int32_t ent[kFirstBatch];
+                resolve_tiles<kFirstBatch>(kp, s, 0, lane, ent);
+                publish(0, kFirstBatch, ent);
+                i0 = kFirstBatch;
+            }
+            for (; i0 < s.ntiles && !stop; i0 += kResolveBatch) {
+                int32_t ent[kResolveBatch];
+                resolve_tiles<kResolveBatch>(kp, s, i0, lane, ent);
+                publish(i0, kResolveBatch, ent);
             }
             g += s.ntiles;
             cur = nxt;
@@ -538,6 +569,10 @@ __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(const KParams 
             const Unit nxt = u + 1 < u_end ? unit_info(kp, sp, u + 1) : cur;   // prefetched
             const Unit &s = cur;
             const bool reload = s.key != prev_key;
+            // the worker's first Q goes out at once, while the resolver still
+            // waits for its first rows; later ones after the unit's first tile
+            const bool q_first = reload && nq == 0;
+            if (q_first && !copy_q(s)) { stop = true; break; }
             for (int i = 0; i < s.ntiles; ++i) {
                 const int gi = g + i, slot = gi % kRing, st = gi & (kStages - 1), use = gi / kStages;
                 if (!warp_wait(bar(B_ROW_FULL + slot), (gi / kRing) & 1, abort_flag)) { stop = true; break; }
@@ -588,9 +623,9 @@ __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(const KParams 
                     pend = gi;
                     pend_vm = vm;
                 }
-                // Q after the unit's first tile: the first tile's row
-                // addresses are the longer dependency chain
-                if (i == 0 && reload && !copy_q(s)) { stop = true; break; }
+                // a reloaded Q after the unit's first tile: that tile's rows
+                // are usually resolved by then, and Q waits for the S issuers
+                if (i == 0 && reload && !q_first && !copy_q(s)) { stop = true; break; }
             }
             g += s.ntiles;
             cur = nxt;
@@ -848,7 +883,8 @@ __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(const KParams 
                 ll = stats_s[2 * h + 1];
             }
             const bool final_split = s.nsplit == 1;
-            const bool ws_ok = final_split || s.w < kp.ws_capacity_splits;
+            const bool ws_ok = final_split || (kp.max_splits > 1 && s.w < kp.max_splits);
+            const int64_t slot = (int64_t)s.t * kp.max_splits + s.w;
             if (!ws_ok && r == 0) set_status(kp, SFM_STATUS_WORKSPACE_OVERFLOW);
             float inv = 0.f;
             if (ll > 0.f) {
@@ -870,7 +906,7 @@ __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(const KParams 
             const int dcol = head_row ? 0 : 256;
             const int hrow = (wl & 1) * 32 + lane;               // this lane's head within the group
             uint16_t *obase = final_split ? static_cast<uint16_t *>(kp.out) + ((int64_t)s.t * kp.q_n + s.h0) * 512
-                                          : kp.ws_o + (int64_t)s.w * kp.q_n * 512;
+                                          : kp.ws_o + slot * kp.q_n * 512;
             const int srow = lane >> 1, spiece = lane & 1;
 #pragma unroll 1
             for (int cc = 0; cc < 8; cc += 2) {
@@ -922,7 +958,7 @@ __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(const KParams 
                 if (final_split) {
                     if (kp.lse) kp.lse[(int64_t)s.t * kp.q_n + s.h0 + h] = lse;
                 } else {
-                    kp.ws_lse[(int64_t)s.w * kp.q_n + s.h0 + h] = lse;
+                    kp.ws_lse[slot * kp.q_n + s.h0 + h] = lse;
                 }
             }
             g += s.ntiles;

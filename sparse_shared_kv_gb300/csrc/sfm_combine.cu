@@ -23,8 +23,8 @@ namespace sfm {
 
 namespace {
 
-constexpr int kThreads = 256;                 // 8 warps, one head each
-constexpr int kHeadsPerBlock = kThreads / 32;
+constexpr int kThreads = 256;                 // 8 warps
+constexpr int kChunksPerRow = 512 / 8;        // 16-byte pieces of a 512-dim row
 
 __device__ __forceinline__ uint32_t to_half2(float a, float b, int dtype)
 {
@@ -38,111 +38,120 @@ __device__ __forceinline__ uint32_t to_half2(float a, float b, int dtype)
 
 constexpr int kUnrolled = 8;                  // splits whose loads are all issued up front
 
-__device__ __forceinline__ void acc_bf16x8(float (&acc)[16], int base, float w, uint4 v)
+__device__ __forceinline__ void acc_bf16x8(float (&acc)[8], float w, uint4 v)
 {
     const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
     for (int e = 0; e < 4; ++e) {      // bf16 pair -> two floats (exact)
-        acc[base + 2 * e] = fmaf(w, __uint_as_float(wv[e] << 16), acc[base + 2 * e]);
-        acc[base + 2 * e + 1] = fmaf(w, __uint_as_float(wv[e] & 0xffff0000u), acc[base + 2 * e + 1]);
+        acc[2 * e] = fmaf(w, __uint_as_float(wv[e] << 16), acc[2 * e]);
+        acc[2 * e + 1] = fmaf(w, __uint_as_float(wv[e] & 0xffff0000u), acc[2 * e + 1]);
     }
 }
 
-// grid (query rows, ceil(q_n / 8)); warp = head, lane = 16 consecutive dims.
-// After the plan words, every load of a row with up to kUnrolled splits goes
-// out at once (the split LSEs, one per lane, and both 16-byte pieces of every
-// split's partial), so the merge costs three dependent round trips.
+// Warps per 16-byte piece of the rows: one lane per head, ceil(q_n / 32)
+// warps cover a piece of every head; a CTA covers 8 / that many pieces.
+__host__ __device__ constexpr int warps_per_piece(int q_n) { return q_n <= 32 ? 1 : q_n <= 64 ? 2 : 4; }
+
+// grid (query rows, 64 / pieces per CTA).  Thread = (head, piece): its loads
+// (the split LSEs of its head, its piece of each split's partial) are
+// coalesced across the warp's 32 heads, since partials are stored
+// chunk-major ([slot][dim / 8][head][8]).  Row t's partials sit in workspace
+// slots t * max_splits + s, so with up to kUnrolled possible splits every load
+// -- plan words, sink, LSEs, pieces -- goes out at once and the merge costs
+// one round trip (slots past the row's split count are loaded, never used).
+// The merged pieces are transposed through shared memory so that each head's
+// output bytes are written contiguously.
 __global__ void __launch_bounds__(kThreads) sfm_combine_kernel(KParams kp)
 {
+    __shared__ uint4 s_out[128 * 8];            // [head][piece of this CTA]
     const int t = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int h = blockIdx.y * kHeadsPerBlock + warp;
+    const int HW = warps_per_piece(kp.q_n), PC = 8 / HW;
+    const int wc = warp / HW;                   // piece within this CTA
+    const int h = (warp - wc * HW) * 32 + lane;
+    const int chunk = blockIdx.y * PC + wc;
     grid_launch_dependents();    // the next launch on the stream may start its set-up
     grid_dependency_wait();      // partial results come from the attention launch before this one
     const int32_t *sp = kp.meta + meta_split_off(kp.G);
     const int32_t sp0 = sp[t], sp1 = sp[t + 1];      // independent of the header check
     const bool ok = meta_ok(kp);
-    if (t == 0 && blockIdx.y == 0 && threadIdx.x == 0) {
+    const bool live = h < kp.q_n;
+    const int hh = live ? h : 0;
+    const int MS = kp.max_splits;
+    const int64_t slot0 = (int64_t)t * MS;
+    const float sink = kp.sinks ? __ldg(kp.sinks + hh) : 0.f;
+    auto piece = [&](int sx) -> const uint4 * {
+        return reinterpret_cast<const uint4 *>(kp.ws_o + (slot0 + sx) * kp.q_n * 512 + ((int64_t)chunk * kp.q_n + hh) * 8);
+    };
+    auto lse_of = [&](int sx) -> float { return kp.ws_lse[(slot0 + sx) * kp.q_n + hh]; };
+    const bool early = MS > 1 && MS <= kUnrolled;
+    float pl[kUnrolled];
+    uint4 v[kUnrolled];
+    if (early) {
+#pragma unroll
+        for (int sx = 0; sx < kUnrolled; ++sx) {
+            pl[sx] = sx < MS ? lse_of(sx) : -INFINITY;
+            v[sx] = sx < MS ? *piece(sx) : make_uint4(0, 0, 0, 0);
+        }
+    }
+    if (t == 0 && blockIdx.y == 0 && threadIdx.x == 0) {     // after this thread's loads are out
         if (!ok) set_status(kp, SFM_STATUS_METADATA_MISMATCH | kp.meta[H_FLAGS]);
         else if (kp.meta[H_LENFLAGS]) set_status(kp, kp.meta[H_LENFLAGS]);
     }
-    if (h >= kp.q_n) return;
-    int ns = 0, s0 = 0;
+    int ns = 0;
     if (ok) {
-        s0 = sp0;
-        ns = sp1 - s0;
-        if (ns == 1) return;      // finalised by the attention kernel
-        if (ns > 1 && (int64_t)s0 + ns > kp.ws_capacity_splits) {
-            if (lane == 0) set_status(kp, SFM_STATUS_WORKSPACE_OVERFLOW);
+        ns = sp1 - sp0;
+        if (ns == 1) return;      // finalised by the attention kernel (uniform over the CTA)
+        if (ns > 1 && ns > MS) {
+            if (threadIdx.x == 0) set_status(kp, SFM_STATUS_WORKSPACE_OVERFLOW);
             ns = 0;
         }
     }
-    const int64_t row = (int64_t)t * kp.q_n + h;
-    // chunk-major partial: [split][dim / 8][head][8]; this lane's 16 dims are
-    // chunks 2 lane and 2 lane + 1
-    auto piece = [&](int sx, int q) -> const uint4 * {
-        return reinterpret_cast<const uint4 *>(kp.ws_o + (int64_t)(s0 + sx) * kp.q_n * 512 +
-                                               ((int64_t)(2 * lane + q) * kp.q_n + h) * 8);
-    };
-    float acc[16];
+    float acc[8];
 #pragma unroll
-    for (int j = 0; j < 16; ++j) acc[j] = 0.f;
+    for (int j = 0; j < 8; ++j) acc[j] = 0.f;
     float L = -INFINITY;
-    if (ns > 0 && ns <= kUnrolled) {
-        const float my_lse = lane < ns ? kp.ws_lse[(int64_t)(s0 + lane) * kp.q_n + h] : -INFINITY;
-        uint4 v[kUnrolled][2];
+    if (ns > 0 && early) {
+        float m = -INFINITY;
 #pragma unroll
         for (int sx = 0; sx < kUnrolled; ++sx)
+            if (sx < ns) m = fmaxf(m, pl[sx]);
+        if (m != -INFINITY) {
+            float z = 0.f;
 #pragma unroll
-            for (int q = 0; q < 2; ++q) v[sx][q] = sx < ns ? *piece(sx, q) : make_uint4(0, 0, 0, 0);
-        float m = my_lse;
-        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-        float z = (m != -INFINITY && lane < ns) ? expf(my_lse - m) : 0.f;
-        for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
-        L = m == -INFINITY ? -INFINITY : m + logf(z);
-        const float wl = (L != -INFINITY && lane < ns) ? expf(my_lse - L) : 0.f;
+            for (int sx = 0; sx < kUnrolled; ++sx)
+                if (sx < ns) z += expf(pl[sx] - m);
+            L = m + logf(z);
 #pragma unroll
-        for (int sx = 0; sx < kUnrolled; ++sx) {
-            const float w = __shfl_sync(0xffffffffu, wl, sx);
-            if (sx < ns) {
-                acc_bf16x8(acc, 0, w, v[sx][0]);
-                acc_bf16x8(acc, 8, w, v[sx][1]);
-            }
+            for (int sx = 0; sx < kUnrolled; ++sx)
+                if (sx < ns) acc_bf16x8(acc, expf(pl[sx] - L), v[sx]);
         }
-    } else if (ns > kUnrolled) {
-        // LSE of the row over its splits: lane s holds split s (in chunks of 32)
+    } else if (ns > 0) {
         float m = -INFINITY;
-        for (int c = 0; c < ns; c += 32)
-            if (c + lane < ns) m = fmaxf(m, kp.ws_lse[(int64_t)(s0 + c + lane) * kp.q_n + h]);
-        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-        float z = 0.f;
-        if (m != -INFINITY)
-            for (int c = 0; c < ns; c += 32)
-                if (c + lane < ns) z += expf(kp.ws_lse[(int64_t)(s0 + c + lane) * kp.q_n + h] - m);
-        for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
-        L = m == -INFINITY ? -INFINITY : m + logf(z);
-        if (L != -INFINITY) {
-            for (int c = 0; c < ns; c += 32) {
-                const int cn = min(32, ns - c);
-                const float wl = lane < cn ? expf(kp.ws_lse[(int64_t)(s0 + c + lane) * kp.q_n + h] - L) : 0.f;
-                for (int sx = 0; sx < cn; ++sx) {
-                    const float w = __shfl_sync(0xffffffffu, wl, sx);
-                    acc_bf16x8(acc, 0, w, *piece(c + sx, 0));
-                    acc_bf16x8(acc, 8, w, *piece(c + sx, 1));
-                }
-            }
+        for (int sx = 0; sx < ns; ++sx) m = fmaxf(m, lse_of(sx));
+        if (m != -INFINITY) {
+            float z = 0.f;
+            for (int sx = 0; sx < ns; ++sx) z += expf(lse_of(sx) - m);
+            L = m + logf(z);
+            for (int sx = 0; sx < ns; ++sx) acc_bf16x8(acc, expf(lse_of(sx) - L), *piece(sx));
         }
     }
     if (L != -INFINITY && kp.sinks) {
-        const float f = 1.f / (1.f + expf(__ldg(kp.sinks + h) - L));
+        const float f = 1.f / (1.f + expf(sink - L));
 #pragma unroll
-        for (int j = 0; j < 16; ++j) acc[j] *= f;
+        for (int j = 0; j < 8; ++j) acc[j] *= f;
     }
-    uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(kp.out) + row * 512 + lane * 16);
-    dst[0] = make_uint4(to_half2(acc[0], acc[1], kp.dtype), to_half2(acc[2], acc[3], kp.dtype),
-                        to_half2(acc[4], acc[5], kp.dtype), to_half2(acc[6], acc[7], kp.dtype));
-    dst[1] = make_uint4(to_half2(acc[8], acc[9], kp.dtype), to_half2(acc[10], acc[11], kp.dtype),
-                        to_half2(acc[12], acc[13], kp.dtype), to_half2(acc[14], acc[15], kp.dtype));
-    if (lane == 0 && kp.lse) kp.lse[row] = L;
+    if (live) {
+        s_out[h * PC + wc] = make_uint4(to_half2(acc[0], acc[1], kp.dtype), to_half2(acc[2], acc[3], kp.dtype),
+                                        to_half2(acc[4], acc[5], kp.dtype), to_half2(acc[6], acc[7], kp.dtype));
+        if (chunk == 0 && kp.lse) kp.lse[(int64_t)t * kp.q_n + h] = L;
+    }
+    __syncthreads();
+    // PC consecutive pieces (16 PC bytes) of one head per group of PC threads
+    uint4 *out = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(kp.out) + (int64_t)t * kp.q_n * 512);
+    for (int i = threadIdx.x; i < kp.q_n * PC; i += kThreads) {
+        const int oh = i / PC, op = i - oh * PC;
+        out[(int64_t)oh * kChunksPerRow + blockIdx.y * PC + op] = s_out[oh * PC + op];
+    }
 }
 
 __global__ void __launch_bounds__(256) sfm_debug_kernel(KParams kp)
@@ -167,7 +176,7 @@ __global__ void __launch_bounds__(256) sfm_debug_kernel(KParams kp)
 cudaError_t launch_combine(const KParams &kp, cudaStream_t st)
 {
     if (kp.T == 0) return cudaSuccess;
-    dim3 grid(kp.T, (kp.q_n + kHeadsPerBlock - 1) / kHeadsPerBlock);
+    dim3 grid(kp.T, kChunksPerRow / (8 / warps_per_piece(kp.q_n)));
     return launch_dependent(sfm_combine_kernel, grid, dim3(kThreads), (size_t)0, st, kp);
 }
 

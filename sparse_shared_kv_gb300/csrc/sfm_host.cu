@@ -214,6 +214,8 @@ void fill_common(KParams &kp, const sfm_params &p, const Plan &pl)
     kp.packed = p.kv_format == SFM_KV_INT8_PACKED;
     kp.ori_bs = p.ori_block_size;
     kp.cmp_bs = p.cmp_block_size;
+    kp.ori_bs_div = make_fastdiv(p.ori_block_size > 0 ? (uint32_t)p.ori_block_size : 1u);
+    kp.cmp_bs_div = make_fastdiv(p.cmp_block_size > 0 ? (uint32_t)p.cmp_block_size : 1u);
     kp.ori_topk = p.ori_topk;
     kp.cmp_topk = p.has_cmp_kv ? p.cmp_topk : 0;
     kp.cmp_ratio = p.cmp_ratio;
@@ -229,6 +231,7 @@ void fill_common(KParams &kp, const sfm_params &p, const Plan &pl)
     kp.fingerprint = (int32_t)fingerprint(p, pl);
     kp.head_groups = head_groups(p, pl);
     kp.wcap = pl.T * pl.max_splits_per_token;
+    kp.max_splits = (int32_t)(pl.max_splits_per_token < INT32_MAX ? pl.max_splits_per_token : INT32_MAX);
 }
 
 void fill_lengths(KParams &kp, const sfm_tensors &t)

@@ -46,11 +46,51 @@ constexpr int kSplitOverheadRows = 128;
 // (rounded up to 32 rows; never more than S when S is a multiple of 32, so
 // the last split is never empty).  Depends on the row's own n and the params
 // only, which keeps results batch invariant.
+// Division by a divisor fixed for the launch (a block size), by
+// multiplication: with l = ceil(log2 d) and M = ceil(2^(32 + l) / d),
+// floor(n M / 2^(32 + l)) = floor(n / d) for every 0 <= n < 2^32 (Granlund and
+// Montgomery, "Division by invariant integers using multiplication", 1994).
+// M < 2^33 is kept as lo + hi 2^32 with hi 0 or 1.
+struct FastDiv {
+    uint32_t lo, hi, l, d;
+};
+
+inline FastDiv make_fastdiv(uint32_t d)
+{
+    FastDiv f{0, 0, 0, d};
+    if (d == 0) return f;
+    while ((1ull << f.l) < d) ++f.l;
+    const uint64_t m = ((1ull << (32 + f.l)) + d - 1) / d;
+    f.lo = (uint32_t)m;
+    f.hi = (uint32_t)(m >> 32);
+    return f;
+}
+
+__device__ __forceinline__ uint32_t fdiv(uint32_t n, const FastDiv &f)
+{
+    const uint64_t t = (uint64_t)__umulhi(n, f.lo) + (f.hi ? n : 0u);
+    return (uint32_t)(t >> f.l);
+}
+
+// a / b for a >= 0, b > 0: a 32-bit division when both fit (64-bit integer
+// division is a long dependent instruction sequence on the GPU)
+__host__ __device__ inline int64_t div_nonneg(int64_t a, int64_t b)
+{
+    if ((((uint64_t)a | (uint64_t)b) >> 32) == 0) return (int64_t)((uint32_t)a / (uint32_t)b);
+    return a / b;
+}
+
+// number of splits of a row with n attended positions
+__host__ __device__ inline int64_t num_splits(int64_t n, int S)
+{
+    return n > 0 ? div_nonneg(n + S - 1, S) : 0;
+}
+
 __host__ __device__ inline int split_size(int64_t n, int S)
 {
     if (n <= 0) return S;
-    const int64_t ns = (n + S - 1) / S;
-    const int64_t sz = (n + ns - 1) / ns;
+    const int64_t ns = num_splits(n, S);
+    const int64_t sz = div_nonneg(n + ns - 1, ns);
     return (int)((sz + 31) & ~(int64_t)31);
 }
 
@@ -87,6 +127,7 @@ struct KParams {
     int32_t ori_max, cmp_max;              // paged: declared max lengths (length capacity)
     int32_t layout_q, layout_kv, dtype, packed;
     int32_t ori_bs, cmp_bs, ori_bt_stride, cmp_bt_stride;
+    FastDiv ori_bs_div, cmp_bs_div;        // division by the block sizes
     int64_t ori_row_stride, cmp_row_stride, ori_rows, cmp_rows;
     int32_t ori_topk, cmp_topk, cmp_ratio, ori_mask_mode, cmp_mask_mode, win_left, win_right;
     int32_t has_cmp, return_lse;
@@ -97,6 +138,8 @@ struct KParams {
     int32_t head_groups;                    // groups of 64 heads (tensor-core path; 1 otherwise): a token
                                             // with n splits owns head_groups * n work units, group-major
     int64_t ws_capacity_splits;
+    int32_t max_splits;                     // splits a row can have: row t's partials use workspace
+                                            // slots t * max_splits .. t * max_splits + max_splits - 1
     int64_t wcap;                           // capacity of the split -> row map
     // tensors
     const void *q;
@@ -108,8 +151,8 @@ struct KParams {
     int32_t *meta_w;
     void *out;
     float *lse;
-    uint16_t *ws_o;   // [capacity][512 / 8][q_n][8] normalised partial O, bf16, chunk-major
-    float *ws_lse;    // [capacity][q_n] partial LSE
+    uint16_t *ws_o;   // [slot][512 / 8][q_n][8] normalised partial O, bf16, chunk-major
+    float *ws_lse;    // [slot][q_n] partial LSE
     int32_t *status;
     int32_t *dbg_rows;
     int64_t dbg_cap;
@@ -220,10 +263,11 @@ __device__ __forceinline__ int64_t phys_row(const KParams &kp, int src, int b, i
     const int bs = src ? kp.cmp_bs : kp.ori_bs;
     const int32_t *bt = src ? kp.cmp_bt : kp.ori_bt;
     const int bts = src ? kp.cmp_bt_stride : kp.ori_bt_stride;
-    if (e / bs >= bts) return -1;     // beyond the block table row
-    const int blk = __ldg(bt + (int64_t)b * bts + e / bs);
+    const int bi = (int)fdiv((uint32_t)e, src ? kp.cmp_bs_div : kp.ori_bs_div);    // e >= 0
+    if (bi >= bts) return -1;     // beyond the block table row
+    const int blk = __ldg(bt + (int64_t)b * bts + bi);
     if (blk < 0) return -1;
-    return (int64_t)blk * bs + e % bs;
+    return (int64_t)blk * bs + (e - bi * bs);
 }
 
 // Resolve attended position `pos` of query row t.  Returns the row address or

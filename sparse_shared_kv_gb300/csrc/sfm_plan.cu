@@ -148,14 +148,14 @@ __global__ void __launch_bounds__(kPlanThreads) sfm_plan_kernel(KParams kp)
     const int beg = min(T, tid * per), end = min(T, beg + per);
     int64_t sum_s = 0, sum_c = 0;
     for (int t = beg; t < end; ++t) {
-        const int64_t n = count(t), ns = n > 0 ? (n + S - 1) / S : 0;
+        const int64_t n = count(t), ns = num_splits(n, S);
         sum_s += ns;
         sum_c += n + ns * kSplitOverheadRows;
     }
     int64_t ex_s = sum_s, ex_c = sum_c;
     block_exclusive_scan2(ex_s, ex_c, s_a, s_b);
     for (int t = beg; t < end; ++t) {
-        const int64_t n = count(t), ns = n > 0 ? (n + S - 1) / S : 0;
+        const int64_t n = count(t), ns = num_splits(n, S);
         if (ex_s > INT32_MAX || ex_c > INT32_MAX || ex_s + ns > kp.wcap) s_overflow = 1;
         sp[t] = (int32_t)ex_s;
         cp[t] = (int32_t)ex_c;
@@ -209,7 +209,7 @@ __global__ void __launch_bounds__(kPlanThreads) sfm_plan_kernel(KParams kp)
         } else if (c == G) {
             u = units;
         } else {
-            const int64_t target = total * c / G;
+            const int64_t target = div_nonneg(total * c, G);
             int lo = 0, hi = T;     // last row t whose cumulative cost <= target
             while (lo < hi) {
                 int mid = (lo + hi + 1) >> 1;
@@ -221,7 +221,7 @@ __global__ void __launch_bounds__(kPlanThreads) sfm_plan_kernel(KParams kp)
                 const int64_t nu = (int64_t)(xsp[lo + 1] - xsp[lo]) * HG;
                 const int64_t within = target - (int64_t)xcp[lo] * HG;
                 const int64_t ucost = split_size(count(lo), S) + kSplitOverheadRows;
-                int64_t k = (within + ucost - 1) / ucost;
+                int64_t k = div_nonneg(within + ucost - 1, ucost);
                 if (k > nu) k = nu;
                 u = (int64_t)xsp[lo] * HG + k;
             }
@@ -236,7 +236,7 @@ __global__ void __launch_bounds__(kPlanThreads) sfm_plan_kernel(KParams kp)
         const int32_t u0 = ws_smem ? s_ws[c] : ws[c], u1 = ws_smem ? s_ws[c + 1] : ws[c + 1];
         int4 *d = reinterpret_cast<int4 *>(wrec + (int64_t)c * kWrecWords);
         d[0] = make_int4(u0, u1, 0, 0);
-        const int64_t w0 = u0 / HG;
+        const int64_t w0 = div_nonneg(u0, HG);
         if (u0 < u1 && w0 < kp.wcap) {
             if (in_smem) {
                 int lo = 0, hi = T - 1;          // the row owning split w0

@@ -74,6 +74,10 @@ def _tiny_cases():
                                          layout_kv="PAGED", mode="csa", cmp_ratio=4, cmp_topk=16, win_left=9,
                                          win_right=0, dtype="fp16", ori_block_size=32, cmp_block_size=16,
                                          sinks=True)))
+    cases.append(("csa_paged_odd_blocks", dict(q_lens=[1, 1], kv_lens=[150, 333], layout_q="BSND",
+                                               layout_kv="PAGED", mode="csa", cmp_ratio=4, cmp_topk=32,
+                                               win_left=20, win_right=0, ori_block_size=48, cmp_block_size=80,
+                                               sinks=True)))
     cases.append(("hca_mode0_bsnd", dict(q_lens=[2], kv_lens=[24], layout_q="BSND", layout_kv="BSND", mode="hca",
                                          cmp_ratio=8, cmp_mask_mode=0, win_left=3, win_right=0)))
     cases.append(("packed_paged", dict(q_lens=[1, 2], kv_lens=[90, 40], layout_q="TND", layout_kv="PAGED",
