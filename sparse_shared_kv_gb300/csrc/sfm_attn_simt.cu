@@ -149,7 +149,7 @@ __global__ void __launch_bounds__(kThreads) sfm_attn_simt_kernel(KParams kp)
         const int sidx = w - sp[t];
         const Tok k = token_info(kp, t);
         const int n = k.n_ori + k.n_cmp;
-        const int size = split_size(n, SR);
+        const int size = split_size_dev(n, kp.split_div);
         const int pos0 = sidx * size;
         const int pos1 = min(n, pos0 + size);
         const bool final_split = nsplit == 1;

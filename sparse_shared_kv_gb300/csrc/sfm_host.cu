@@ -214,6 +214,9 @@ void fill_common(KParams &kp, const sfm_params &p, const Plan &pl)
     kp.packed = p.kv_format == SFM_KV_INT8_PACKED;
     kp.ori_bs = p.ori_block_size;
     kp.cmp_bs = p.cmp_block_size;
+    kp.q_s_div = make_fastdiv(kp.q_s > 0 ? (uint32_t)kp.q_s : 1u);
+    kp.ratio_div = make_fastdiv(p.cmp_ratio > 0 ? (uint32_t)p.cmp_ratio : 1u);
+    kp.split_div = make_fastdiv(pl.split_rows > 0 ? (uint32_t)pl.split_rows : 1u);
     kp.ori_bs_div = make_fastdiv(p.ori_block_size > 0 ? (uint32_t)p.ori_block_size : 1u);
     kp.cmp_bs_div = make_fastdiv(p.cmp_block_size > 0 ? (uint32_t)p.cmp_block_size : 1u);
     kp.ori_topk = p.ori_topk;

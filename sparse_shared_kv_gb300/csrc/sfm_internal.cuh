@@ -94,16 +94,45 @@ __host__ __device__ inline int split_size(int64_t n, int S)
     return (int)((sz + 31) & ~(int64_t)31);
 }
 
+// floor(a / b) for 32-bit a, b >= 1: a float estimate (32-bit conversions
+// are cheap, 64-bit ones and integer division are not) corrected exactly; the
+// estimate is within one of the quotient whenever a < 2^24, and an estimate
+// that needs more than two corrections falls back to the division
+__device__ __forceinline__ uint32_t udiv_est(uint32_t a, uint32_t b)
+{
+    uint32_t q = __float2uint_rz(__fdividef(__uint2float_rz(a), __uint2float_rz(b)));
+    if ((uint64_t)q * b > a) --q;
+    else if (((uint64_t)q + 1) * b <= a) ++q;
+    if ((uint64_t)q * b > a || ((uint64_t)q + 1) * b <= a) q = a / b;
+    return q;
+}
+
+// num_splits / split_size with the launch's precomputed division by split_rows
+__device__ __forceinline__ int64_t num_splits_dev(int64_t n, const FastDiv &sd)
+{
+    if (n <= 0) return 0;
+    const int64_t a = n + sd.d - 1;
+    return a <= 0xffffffffll ? (int64_t)fdiv((uint32_t)a, sd) : a / sd.d;
+}
+__device__ __forceinline__ int split_size_dev(int64_t n, const FastDiv &sd)
+{
+    if (n <= 0) return (int)sd.d;
+    const int64_t ns = num_splits_dev(n, sd);
+    const int64_t a = n + ns - 1;
+    const int64_t sz = ns == 1 ? n : a <= 0xffffffffll ? (int64_t)udiv_est((uint32_t)a, (uint32_t)ns) : a / ns;
+    return (int)((sz + 31) & ~(int64_t)31);
+}
+
 __host__ __device__ inline int64_t meta_ws_off() { return kHdr; }
 __host__ __device__ inline int64_t meta_split_off(int G) { return kHdr + (int64_t)G + 1; }
 __host__ __device__ inline int64_t meta_cost_off(int G, int T) { return kHdr + (int64_t)G + 1 + (int64_t)T + 1; }
 __host__ __device__ inline int64_t meta_rec_off(int G, int T) { return meta_cost_off(G, T) + (int64_t)T + 1; }
-__host__ __device__ inline int64_t meta_own_off(int G, int T) { return meta_rec_off(G, T) + (int64_t)kRecWords * T; }
 constexpr int kSrecWords = 16;
 constexpr int kWrecWords = 32;
 __host__ __device__ inline int64_t meta_srec_off(int G, int T, int64_t wcap)
 {
-    return (meta_own_off(G, T) + wcap + 15) & ~(int64_t)15;
+    (void)wcap;
+    return (meta_rec_off(G, T) + (int64_t)kRecWords * T + 15) & ~(int64_t)15;
 }
 __host__ __device__ inline int64_t meta_wrec_off(int G, int T, int64_t wcap)
 {
@@ -128,6 +157,7 @@ struct KParams {
     int32_t layout_q, layout_kv, dtype, packed;
     int32_t ori_bs, cmp_bs, ori_bt_stride, cmp_bt_stride;
     FastDiv ori_bs_div, cmp_bs_div;        // division by the block sizes
+    FastDiv q_s_div, ratio_div, split_div; // by q_s, cmp_ratio and split_rows
     int64_t ori_row_stride, cmp_row_stride, ori_rows, cmp_rows;
     int32_t ori_topk, cmp_topk, cmp_ratio, ori_mask_mode, cmp_mask_mode, win_left, win_right;
     int32_t has_cmp, return_lse;
@@ -187,7 +217,7 @@ __device__ inline Tok token_info(const KParams &kp, int t)
     Tok k;
     int32_t qcap;
     if (kp.layout_q == SFM_LAYOUT_BSND) {
-        k.b = t / kp.q_s;
+        k.b = (int)fdiv((uint32_t)t, kp.q_s_div);
         k.i = t - k.b * kp.q_s;
         qcap = kp.q_s;
     } else {
@@ -244,7 +274,9 @@ __device__ inline Tok token_info(const KParams &kp, int t)
         if (kp.cmp_topk > 0) {
             k.n_cmp = kp.cmp_topk;
         } else if (kp.cmp_mask_mode == 3) {
-            int64_t v = (pc + 1) >= 0 ? (pc + 1) / kp.cmp_ratio : 0;   // slots j with (j+1)*ratio <= pc+1
+            // slots j with (j+1)*ratio <= pc+1
+            int64_t v = (pc + 1) < 0 ? 0 : (pc + 1) <= 0xffffffffll ? (int64_t)fdiv((uint32_t)(pc + 1), kp.ratio_div)
+                                                                    : (pc + 1) / kp.cmp_ratio;
             k.n_cmp = (int32_t)(v < k.cmp_len ? v : k.cmp_len);
         } else {
             k.n_cmp = k.cmp_len;

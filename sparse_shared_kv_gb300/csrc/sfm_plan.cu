@@ -8,24 +8,27 @@
 //     ceil(n_t / split_rows) equal splits -- a function of the row's own count and
 //     the params only, so a row's arithmetic never depends on the rest of the
 //     batch (the 确定性计算 section makes batch invariance the default);
-//   * per query row: the lengths / window / position counts the attention
-//     kernels need (so they skip the length walk), and the split -> row map;
-//   * per worker (persistent CTA): a contiguous range of splits chosen so that
-//     every worker gets about the same modelled cost (attended rows plus a
-//     fixed per-split latency cost).
+//   * per split: a 64-byte record with its row, the row's split count and
+//     size, and the lengths / window / position counts the attention kernels
+//     need (so they skip the length walk);
+//   * per worker (persistent CTA): a contiguous range of work units chosen so
+//     that every worker gets about the same modelled cost (attended rows plus
+//     a fixed per-split latency cost), and its first unit's split record.
 // Each row's lengths are read once (phase 1, one row per thread); the prefix
 // sums (phase 2, contiguous runs per thread) recompute the counts from the
-// per-row records, and the worker searches (phase 3) run on shared-memory
-// copies of the prefixes when the rows fit.
+// per-row records; phase 3 writes the split and worker records in parallel
+// (binary searches over shared-memory copies of the prefixes when the rows
+// fit).  Every step after the length loads is a short chain per thread: the
+// planner sits on the critical path of a decode step.
 #include "sfm_internal.cuh"
 
 namespace sfm {
 
 namespace {
 
-constexpr int kPlanThreads = 1024;
-constexpr int kSmemRows = 1024;          // rows whose records and prefixes stay in shared memory
-constexpr int kMaxWorkers = 256;
+constexpr int kPlanThreads = 512;
+constexpr int kSmemRows = 512;           // rows whose records stay in shared memory
+constexpr int kMaxWorkers = 256;         // persistent workers (one per SM)
 
 // Exclusive prefix sums of two values per thread over the block: a shuffle
 // scan inside each warp, then one warp scans the 32 warp totals.
@@ -73,17 +76,22 @@ __device__ __forceinline__ void block_exclusive_scan2(int64_t &a, int64_t &b, in
     __syncthreads();
 }
 
-// One CTA.  Rows up to kSmemRows keep their records and prefixes in shared
-// memory, so after the length loads of phase 1 every phase reads shared
-// memory only (no global write-then-read round trips).
+// One CTA.  Rows up to kSmemRows keep their records in shared memory, so
+// after the length loads of phase 1 no phase reads global memory.  No thread
+// runs a serial chain longer than its rows' splits and worker boundaries: the
+// planner sits on the critical path of a decode step.
 __global__ void __launch_bounds__(kPlanThreads) sfm_plan_kernel(KParams kp)
 {
     __shared__ int64_t s_a[32];
     __shared__ int64_t s_b[32];
     __shared__ int4 s_rec[kSmemRows][2];
-    __shared__ int32_t s_sp[kSmemRows + 1];
-    __shared__ int32_t s_cp[kSmemRows + 1];
-    __shared__ int32_t s_ws[kMaxWorkers + 1];
+    __shared__ int2 s_shape[kSmemRows];           // splits, split size
+    __shared__ int32_t s_sp[kSmemRows];           // first split of each row
+    __shared__ int32_t s_cp[kSmemRows];           // modelled cost before each row
+    __shared__ int32_t s_ws[kMaxWorkers + 1];     // worker c's first unit
+    __shared__ int32_t s_wrow[kMaxWorkers];       // the row of that unit
+    __shared__ int32_t s_wbeg[kMaxWorkers];       // the row's first split
+    __shared__ int64_t s_tot[2];                  // splits, modelled cost
     __shared__ int s_overflow;
 
     // the attention kernel may start its set-up now; it waits for this grid
@@ -99,14 +107,13 @@ __global__ void __launch_bounds__(kPlanThreads) sfm_plan_kernel(KParams kp)
     int32_t *sp = meta + meta_split_off(G);
     int32_t *cp = meta + meta_cost_off(G, T);
     int32_t *rec = meta + meta_rec_off(G, T);
-    int32_t *own = meta + meta_own_off(G, T);
     int32_t *srec = meta + meta_srec_off(G, T, kp.wcap);
     int32_t *wrec = meta + meta_wrec_off(G, T, kp.wcap);
     const bool in_smem = T <= kSmemRows;
-    const bool ws_smem = G <= kMaxWorkers;
     const int tid = threadIdx.x;
     if (tid == 0) {
-        s_overflow = 0;
+        s_overflow = G > kMaxWorkers ? 1 : 0;
+        s_tot[0] = s_tot[1] = 0;
         meta[H_LENFLAGS] = 0;       // length problems found while planning are OR-ed here
     }
     __syncthreads();
@@ -116,16 +123,30 @@ __global__ void __launch_bounds__(kPlanThreads) sfm_plan_kernel(KParams kp)
         if (in_smem) {
             r0 = s_rec[t][0];
             r1 = s_rec[t][1];
-        } else {
+        } else {                         // 4-byte aligned only: scalar accesses
             const int32_t *r = rec + (int64_t)kRecWords * t;
             r0 = make_int4(r[0], r[1], r[2], r[3]);
             r1 = make_int4(r[4], r[5], r[6], r[7]);
         }
     };
-    auto count = [&](int t) -> int64_t {
-        int4 r0, r1;
-        rec_of(t, r0, r1);
-        return (int64_t)r1.z + r1.w;     // n_ori + n_cmp
+    const int64_t HG = kp.head_groups;
+    // a row's splits, their size and the modelled cost of each of its
+    // head_groups * splits work units (rows plus a fixed per-unit latency cost)
+    auto shape_of = [&](int64_t n) -> int2 {           // n = n_ori + n_cmp
+        return make_int2((int)num_splits_dev(n, kp.split_div), split_size_dev(n, kp.split_div));
+    };
+    auto row_shape = [&](int t, int64_t &ns, int &size, int64_t &ucost) {
+        int2 sh;
+        if (in_smem) {
+            sh = s_shape[t];
+        } else {
+            int4 r0, r1;
+            rec_of(t, r0, r1);
+            sh = shape_of((int64_t)r1.z + r1.w);
+        }
+        ns = sh.x;
+        size = sh.y;
+        ucost = size + kSplitOverheadRows;
     };
 
     // 1. every row once: lengths, window and position counts
@@ -135,6 +156,7 @@ __global__ void __launch_bounds__(kPlanThreads) sfm_plan_kernel(KParams kp)
         if (in_smem) {
             s_rec[t][0] = r0;
             s_rec[t][1] = r1;
+            s_shape[t] = shape_of((int64_t)k.n_ori + k.n_cmp);
         } else {
             int32_t *r = rec + (int64_t)kRecWords * t;
             r[0] = r0.x; r[1] = r0.y; r[2] = r0.z; r[3] = r0.w;
@@ -142,122 +164,144 @@ __global__ void __launch_bounds__(kPlanThreads) sfm_plan_kernel(KParams kp)
         }
     }
     __syncthreads();
-    // 2. split / cost prefixes: each thread scans a contiguous run of rows and
-    //    writes the split records of its rows
+
+    // 2. split and unit-cost prefixes over contiguous runs of rows per thread
     const int per = (T + kPlanThreads - 1) / kPlanThreads;
     const int beg = min(T, tid * per), end = min(T, beg + per);
     int64_t sum_s = 0, sum_c = 0;
     for (int t = beg; t < end; ++t) {
-        const int64_t n = count(t), ns = num_splits(n, S);
+        int64_t ns, ucost;
+        int size;
+        row_shape(t, ns, size, ucost);
         sum_s += ns;
-        sum_c += n + ns * kSplitOverheadRows;
+        sum_c += ns * HG * ucost;
     }
     int64_t ex_s = sum_s, ex_c = sum_c;
     block_exclusive_scan2(ex_s, ex_c, s_a, s_b);
-    for (int t = beg; t < end; ++t) {
-        const int64_t n = count(t), ns = num_splits(n, S);
-        if (ex_s > INT32_MAX || ex_c > INT32_MAX || ex_s + ns > kp.wcap) s_overflow = 1;
+    for (int t = beg; t < end; ++t) {     // per-row prefixes: the split table (global) and cost prefix
+        int64_t ns, ucost;
+        int size;
+        row_shape(t, ns, size, ucost);
+        if (ex_s > INT32_MAX || ex_c > INT32_MAX || ns > kp.max_splits) s_overflow = 1;
         sp[t] = (int32_t)ex_s;
-        cp[t] = (int32_t)ex_c;
         if (in_smem) {
             s_sp[t] = (int32_t)ex_s;
             s_cp[t] = (int32_t)ex_c;
+        } else {
+            cp[t] = (int32_t)ex_c;
         }
-        if (ns > 0) {
+        ex_s += ns;
+        ex_c += ns * HG * ucost;
+    }
+    if (beg < end && end == T) {          // the run that ends the rows holds the totals
+        s_tot[0] = ex_s;
+        s_tot[1] = ex_c;
+    }
+    __syncthreads();
+    const int64_t W = s_tot[0], units = W * HG, total = s_tot[1];
+    if (tid == 0 && (W > INT32_MAX || units > INT32_MAX || W > kp.wcap || total > INT32_MAX)) s_overflow = 1;
+    auto sp_of = [&](int t) -> int64_t { return in_smem ? s_sp[t] : sp[t]; };
+    auto cp_of = [&](int t) -> int64_t { return in_smem ? s_cp[t] : cp[t]; };
+
+    // 3. two independent halves of the block, so that neither chain waits for
+    //    the other:
+    //    (a) threads [0, kHalf): each row's 64-byte split records;
+    //    (b) threads [kHalf, 2 kHalf): the worker boundaries in each row.  A
+    //        row's units are group-major (unit hg * ns + s is split s for head
+    //        group hg), so consecutive units of a worker mostly share their Q
+    //        rows.  Unit j of row t spans modelled cost [cp(t) + j ucost,
+    //        cp(t) + (j + 1) ucost); worker c starts at the unit whose span
+    //        holds target(c) = floor(c total / G), so every worker gets about
+    //        the same cost.  The workers whose targets fall in the row and
+    //        their units come from three divisions per row and a merge walk.
+    constexpr int kHalf = kPlanThreads / 2;
+    if (tid < kHalf) {
+        for (int t = tid; t < T; t += kHalf) {
+            int64_t ns, ucost;
+            int size;
+            row_shape(t, ns, size, ucost);
             int4 r0, r1;
             rec_of(t, r0, r1);
-            const int4 hd = make_int4(t, (int32_t)ex_s, (int32_t)ns, split_size(n, S));
-            for (int64_t j = 0; j < ns && ex_s + j < kp.wcap; ++j) {
-                own[ex_s + j] = t;
-                int4 *d = reinterpret_cast<int4 *>(srec + (ex_s + j) * kSrecWords);
+            const int64_t s0 = sp_of(t);
+            const int4 hd = make_int4(t, (int32_t)s0, (int32_t)ns, size);
+            for (int64_t j = 0; j < ns && s0 + j < kp.wcap; ++j) {
+                int4 *d = reinterpret_cast<int4 *>(srec + (s0 + j) * kSrecWords);
                 d[0] = hd;
                 d[1] = r0;
                 d[2] = r1;
                 d[3] = make_int4(0, 0, 0, 0);
             }
         }
-        ex_s += ns;
-        ex_c += n + ns * kSplitOverheadRows;
-    }
-    if ((beg < end && end == T) || (T == 0 && tid == 0)) {   // the run that ends the rows writes the totals
-        if (ex_s > INT32_MAX || ex_c > INT32_MAX) s_overflow = 1;
-        sp[T] = (int32_t)ex_s;
-        cp[T] = (int32_t)ex_c;
-        if (in_smem) {
-            s_sp[T] = (int32_t)ex_s;
-            s_cp[T] = (int32_t)ex_c;
+        if (tid == 0) sp[T] = (int32_t)(W < INT32_MAX ? W : INT32_MAX);
+    } else if (total > 0) {
+        const bool small = (total + 1) * (G + 1) <= 0xffffffffll;     // boundary arithmetic fits 32 bits
+        auto qdiv = [&](int64_t a, int64_t b) -> int64_t {
+            return small ? (int64_t)udiv_est((uint32_t)a, (uint32_t)b) : a / b;
+        };
+        const int64_t tq = qdiv(total, G), tr = total - tq * G;      // target(c + 1) - target(c) = tq or tq + 1
+        for (int t = tid - kHalf; t < T; t += kHalf) {
+            int64_t ns, ucost;
+            int size;
+            row_shape(t, ns, size, ucost);
+            const int64_t nu = ns * HG, c0 = cp_of(t), s0 = sp_of(t);
+            if (nu == 0) continue;
+            // workers c with c0 <= target(c) < c0 + nu ucost
+            const int64_t c_first = qdiv(c0 * G + total - 1, total);
+            int64_t c_end = qdiv((c0 + nu * ucost) * G + total - 1, total);
+            if (c_end > G) c_end = G;
+            if (c_first >= c_end) continue;
+            const int64_t num = c_first * total;
+            int64_t tgt = qdiv(num, G), rem = num - tgt * G;
+            int64_t j = 0, ustart = c0;
+            for (int64_t c = c_first; c < c_end; ++c) {
+                while (j + 1 < nu && ustart + ucost <= tgt) {
+                    ustart += ucost;
+                    ++j;
+                }
+                if (c < kMaxWorkers) {
+                    s_ws[c] = (int32_t)(s0 * HG + j);
+                    s_wrow[c] = t;
+                    s_wbeg[c] = (int32_t)s0;
+                }
+                tgt += tq;
+                rem += tr;
+                if (rem >= G) {
+                    rem -= G;
+                    ++tgt;
+                }
+            }
         }
+    }
+    if (tid == kHalf) {
+        if (G <= kMaxWorkers) s_ws[G] = (int32_t)(units < INT32_MAX ? units : INT32_MAX);
+        if (total == 0)                   // no work: every worker's range is empty
+            for (int c = 0; c < G && c < kMaxWorkers; ++c) {
+                s_ws[c] = 0;
+                s_wrow[c] = 0;
+                s_wbeg[c] = 0;
+            }
     }
     __syncthreads();
 
-    // 3. worker ranges over work units: a unit is one split for one group of
-    //    heads; row t owns units [sp[t] * HG, sp[t+1] * HG), group-major, so
-    //    that consecutive units of a worker mostly share their Q rows.  Worker
-    //    c starts at the first unit whose cumulative cost reaches c / G of the
-    //    total.
-    const int32_t *xsp = in_smem ? s_sp : sp;
-    const int32_t *xcp = in_smem ? s_cp : cp;
-    const int64_t HG = kp.head_groups;
-    const int32_t W = xsp[T];
-    const int64_t units = (int64_t)W * HG;
-    if (units > INT32_MAX && tid == 0) s_overflow = 1;
-    const int64_t total = (int64_t)xcp[T] * HG;
-    for (int c = tid; c <= G; c += kPlanThreads) {
-        int64_t u;
-        if (c == 0) {
-            u = 0;
-        } else if (c == G) {
-            u = units;
-        } else {
-            const int64_t target = div_nonneg(total * c, G);
-            int lo = 0, hi = T;     // last row t whose cumulative cost <= target
-            while (lo < hi) {
-                int mid = (lo + hi + 1) >> 1;
-                if ((int64_t)xcp[mid] * HG <= target) lo = mid; else hi = mid - 1;
-            }
-            if (lo >= T) {
-                u = units;
-            } else {
-                const int64_t nu = (int64_t)(xsp[lo + 1] - xsp[lo]) * HG;
-                const int64_t within = target - (int64_t)xcp[lo] * HG;
-                const int64_t ucost = split_size(count(lo), S) + kSplitOverheadRows;
-                int64_t k = div_nonneg(within + ucost - 1, ucost);
-                if (k > nu) k = nu;
-                u = (int64_t)xsp[lo] * HG + k;
-            }
-        }
-        const int32_t v = (int32_t)(u < INT32_MAX ? u : INT32_MAX);
-        ws[c] = v;
-        if (ws_smem) s_ws[c] = v;
-    }
-    __syncthreads();
-    // 4. per worker: its range and its first unit's split record in one place
-    for (int c = tid; c < G; c += kPlanThreads) {
-        const int32_t u0 = ws_smem ? s_ws[c] : ws[c], u1 = ws_smem ? s_ws[c + 1] : ws[c + 1];
+    // 4. per worker: its range and its first unit's row record in one place
+    for (int c = tid; c <= G && c <= kMaxWorkers; c += kPlanThreads) {
+        const int32_t u0 = s_ws[c];
+        ws[c] = u0;
+        if (c == G) break;
+        const int32_t u1 = s_ws[c + 1];
         int4 *d = reinterpret_cast<int4 *>(wrec + (int64_t)c * kWrecWords);
         d[0] = make_int4(u0, u1, 0, 0);
-        const int64_t w0 = div_nonneg(u0, HG);
-        if (u0 < u1 && w0 < kp.wcap) {
-            if (in_smem) {
-                int lo = 0, hi = T - 1;          // the row owning split w0
-                while (lo < hi) {
-                    int mid = (lo + hi + 1) >> 1;
-                    if (s_sp[mid] <= w0) lo = mid; else hi = mid - 1;
-                }
-                const int64_t n = count(lo), ns = s_sp[lo + 1] - s_sp[lo];
-                int4 r0, r1;
-                rec_of(lo, r0, r1);
-                d[1] = make_int4(lo, s_sp[lo], (int32_t)ns, split_size(n, S));
-                d[2] = r0;
-                d[3] = r1;
-                d[4] = make_int4(0, 0, 0, 0);
-            } else {
-                const int4 *src = reinterpret_cast<const int4 *>(srec + w0 * kSrecWords);
-                d[1] = src[0];
-                d[2] = src[1];
-                d[3] = src[2];
-                d[4] = src[3];
-            }
+        if (u0 < u1) {
+            const int t = s_wrow[c];
+            int64_t ns, ucost;
+            int size;
+            row_shape(t, ns, size, ucost);
+            int4 r0, r1;
+            rec_of(t, r0, r1);
+            d[1] = make_int4(t, s_wbeg[c], (int32_t)ns, size);
+            d[2] = r0;
+            d[3] = r1;
+            d[4] = make_int4(0, 0, 0, 0);
         }
     }
     if (tid == 0) {
@@ -267,7 +311,7 @@ __global__ void __launch_bounds__(kPlanThreads) sfm_plan_kernel(KParams kp)
         meta[H_WORKERS] = G;
         meta[H_SPLIT] = S;
         meta[H_PATH] = kp.path;
-        meta[H_TOTAL_SPLITS] = W;
+        meta[H_TOTAL_SPLITS] = (int32_t)(W < INT32_MAX ? W : INT32_MAX);
         meta[H_FLAGS] = s_overflow ? SFM_STATUS_PLAN_OVERFLOW : 0;
         meta[H_WCAP] = (int32_t)(kp.wcap < INT32_MAX ? kp.wcap : INT32_MAX);
         for (int j = 10; j < kHdr; ++j) meta[j] = 0;
