@@ -451,7 +451,7 @@ def run_e2e(args, sfm, sets, acc, dev, stream):
             ori_row_stride=p.ori_row_stride, cmp_row_stride=p.cmp_row_stride or None, out=out, lse=lse,
             stream=st)
 
-    legs = []
+    legs, keep = [], []          # the graphs, and every buffer their nodes point at
     h2d = d2h = 0
     for i, p in enumerate(sets):
         parts = [(n, p.t[n]) for n in names if p.t[n] is not None]
@@ -491,6 +491,7 @@ def run_e2e(args, sfm, sets, acc, dev, stream):
             api_step(p, T, out, lse, st)
             ohost.copy_(obuf, non_blocking=True)
         legs.append(g)
+        keep.append((hbuf, dbuf, obuf, ohost, T, out, lse))
     torch.cuda.synchronize()
     streams = [torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)]
 
