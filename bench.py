@@ -39,7 +39,8 @@ sys.path.insert(0, ROOT)
 
 import torch  # noqa: E402
 
-WORKLOADS = ("csa_decode", "hca_decode", "packed_decode", "csa_prefill")
+WORKLOADS = ("csa_decode", "hca_decode", "packed_decode", "packed_fp8_decode", "csa_prefill")
+S_KV_FORMAT_CODES = {"plain": 0, "int8_packed": 1, "fp8_packed": 2}     # sfm_params.kv_format
 
 
 def parse():
@@ -381,7 +382,8 @@ def run_ours(args):
             "higher_is_better": True,
             "scaling": "weak",
             "vs_baseline": None,
-            "dtype": "fp16 (int8 KV dequantized)" if p0.kv_format == "int8_packed" else "bf16",
+            "dtype": {"int8_packed": "fp16 (int8 KV dequantized)", "fp8_packed": "fp16 (fp8 e4m3 KV dequantized)"}
+                     .get(p0.kv_format, "bf16"),
             "data": "synthetic (seeded generators, shapes and distributions of the pages' workloads)",
             "config": {
                 "workload": args.workload, "batch": p0.batch_size, "q_n": p0.num_heads_q, "d": 512,
@@ -438,7 +440,7 @@ def run_e2e(args, sfm, sets, acc, dev, stream):
             cmp_ratio=p.cmp_ratio, ori_mask_mode=p.ori_mask_mode, cmp_mask_mode=p.cmp_mask_mode,
             ori_win_left=p.ori_win_left, ori_win_right=p.ori_win_right, layout_q=p.layout_q,
             layout_kv=p.layout_kv, has_cmp_kv=p.has_cmp_kv, dtype=p.torch_dtype,
-            kv_format=1 if p.kv_format == "int8_packed" else 0, rope_head_dim=p.rope_head_dim,
+            kv_format=S_KV_FORMAT_CODES[p.kv_format], rope_head_dim=p.rope_head_dim,
             ori_block_size=p.ori_block_size, cmp_block_size=p.cmp_block_size, return_softmax_lse=True,
             device=dev, stream=st)
         sfm.sparse_flash_mla(

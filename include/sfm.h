@@ -82,8 +82,13 @@ enum sfm_dtype { SFM_DTYPE_BF16 = 0, SFM_DTYPE_FP16 = 1 };
  *                       one per 128-dim tile: 656 bytes (rope 64) or 528 bytes
  *                       (rope 0).  K~[d] = int8[d] * scale[d / 128] for
  *                       d < 512, followed by the rope values; V~ = K~[0:512];
- *                       q has 512 + rope_head_dim dims, out has 512. */
-enum sfm_kv_format { SFM_KV_PLAIN = 0, SFM_KV_INT8_PACKED = 1 };
+ *                       q has 512 + rope_head_dim dims, out has 512.
+ *   SFM_KV_FP8_PACKED   the same guide, "Ascend 950 INT8/FP8 C8 NoPE" section:
+ *                       the same 528 / 656-byte rows with the 512 NoPE bytes
+ *                       FLOAT8_E4M3FN values (sign, 4 exponent bits biased by
+ *                       7, 3 mantissa bits, no infinity, S.1111.111 = NaN):
+ *                       K~[d] = e4m3(byte d) * scale[d / 128]. */
+enum sfm_kv_format { SFM_KV_PLAIN = 0, SFM_KV_INT8_PACKED = 1, SFM_KV_FP8_PACKED = 2 };
 
 /* Host-side return codes. */
 enum sfm_error {

@@ -81,6 +81,8 @@ def _configure(l):
     l.oracle_attended.argtypes = [C.POINTER(OracleProblem), C.c_int32, C.c_void_p, C.c_void_p, C.c_int64]
     l.oracle_token_info.restype = C.c_int
     l.oracle_token_info.argtypes = [C.POINTER(OracleProblem), C.c_int32, C.c_void_p]
+    l.oracle_dec_e4m3.restype = C.c_double
+    l.oracle_dec_e4m3.argtypes = [C.c_int32]
     return l
 
 
@@ -139,7 +141,7 @@ class _Bound:
         s.layout_q = _LAYOUT[prob.layout_q]
         s.layout_kv = _LAYOUT[prob.layout_kv]
         s.dtype = 0 if prob.dtype == "bf16" else 1
-        s.kv_packed = 1 if prob.kv_format == "int8_packed" else 0
+        s.kv_packed = {"int8_packed": 1, "fp8_packed": 2}.get(prob.kv_format, 0)
         s.ori_bs = prob.ori_block_size
         s.cmp_bs = prob.cmp_block_size
         ori = t["ori_kv"]
@@ -217,6 +219,11 @@ def attended(prob, token: int, _bound: Optional[_Bound] = None):
 def attended_all(prob):
     b = _Bound(prob)
     return [attended(prob, t, b) for t in range(prob.num_tokens)]
+
+
+def dec_e4m3(code: int) -> float:
+    """The oracle's FLOAT8_E4M3FN decoder for one byte (for its pins)."""
+    return lib().oracle_dec_e4m3(int(code))
 
 
 def token_info(prob, token: int):

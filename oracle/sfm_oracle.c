@@ -45,6 +45,9 @@
  *   packed rows: k[d] = int8[d] * scale[d / 128] for d < 512, then the rope
  *   values; V = k[0:512] (kv_quant_sparse_flash_attention guide, 计算公式 and
  *   the "A2/A3 C8 NoPE" table: 512 int8 + 64 rope + 4 fp32 scales = 656 B).
+ *   FP8 packed rows (the guide's "Ascend 950 INT8/FP8 C8 NoPE" section, same
+ *   528 / 656-byte layout): the 512 NoPE bytes are FLOAT8_E4M3FN values,
+ *   k[d] = e4m3(byte d) * scale[d / 128].
  */
 #include <math.h>
 #include <stdint.h>
@@ -100,6 +103,20 @@ static double dec_fp16(uint16_t h)
 static double dec_half(const oracle_problem *P, uint16_t h)
 {
     return P->dtype == 0 ? dec_bf16(h) : dec_fp16(h);
+}
+
+/* FLOAT8_E4M3FN (the OCP 8-bit floating point format the kv_quant guide names
+ * for its A5 rows): sign bit, 4 exponent bits with bias 7, 3 mantissa bits;
+ * exponent 0 is subnormal (m/8 * 2^-6); exponent 15 with mantissa 7 is NaN
+ * and there is no infinity, so the largest finite value is 1.75 * 2^8 = 448. */
+static double dec_e4m3(uint8_t b)
+{
+    int s = b >> 7, e = (b >> 3) & 15, m = b & 7;
+    double v;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0) v = ldexp((double)m, -9);
+    else v = ldexp((double)(m + 8), e - 10);
+    return s ? -v : v;
 }
 
 /* ---------------- per-token lengths and position ---------------- */
@@ -250,7 +267,10 @@ static void decode_row(const oracle_problem *P, const uint8_t *r, double *k)
     }
     float scale[4];
     memcpy(scale, r + 512 + 2 * P->rope_dim, 16);
-    for (int d = 0; d < 512; ++d) k[d] = (double)(int8_t)r[d] * (double)scale[d / 128];
+    if (P->kv_packed == 2)
+        for (int d = 0; d < 512; ++d) k[d] = dec_e4m3(r[d]) * (double)scale[d / 128];
+    else
+        for (int d = 0; d < 512; ++d) k[d] = (double)(int8_t)r[d] * (double)scale[d / 128];
     for (int j = 0; j < P->rope_dim; ++j) {
         uint16_t h;
         memcpy(&h, r + 512 + 2 * j, 2);
@@ -259,6 +279,9 @@ static void decode_row(const oracle_problem *P, const uint8_t *r, double *k)
 }
 
 /* ---------------- exported API ---------------- */
+/* the E4M3 decoder on its own, for the tests that pin it */
+double oracle_dec_e4m3(int32_t code) { return dec_e4m3((uint8_t)code); }
+
 int oracle_token_info(const oracle_problem *P, int32_t t, int32_t *out9)
 {
     tok_info ti;

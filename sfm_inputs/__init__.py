@@ -31,6 +31,8 @@ from typing import Dict, List, Optional, Sequence
 import torch
 
 PACKED_ROW_BYTES = 656      # 512 int8 + 64 * 2 rope + 4 * 4 scales
+KV_FORMAT_CODES = {"plain": 0, "int8_packed": 1, "fp8_packed": 2}
+PACKED_FORMATS = ("int8_packed", "fp8_packed")
 PACKED_ROW_BYTES_ROPE0 = 528
 HEAD_DIM = 512
 
@@ -63,7 +65,7 @@ class Problem:
     has_ori_kv: bool
     has_cmp_kv: bool
     dtype: str                    # 'bf16' | 'fp16'
-    kv_format: str                # 'plain' | 'int8_packed'
+    kv_format: str                # 'plain' | 'int8_packed' | 'fp8_packed'
     ori_block_size: int
     cmp_block_size: int
     return_lse: bool
@@ -89,8 +91,12 @@ class Problem:
     def torch_dtype(self) -> torch.dtype:
         return torch.bfloat16 if self.dtype == "bf16" else torch.float16
 
+    @property
+    def packed(self) -> bool:
+        return self.kv_format in PACKED_FORMATS
+
     def kv_row_bytes(self) -> int:
-        if self.kv_format == "int8_packed":
+        if self.packed:
             return PACKED_ROW_BYTES if self.rope_head_dim == 64 else PACKED_ROW_BYTES_ROPE0
         return self.head_dim * 2
 
@@ -111,7 +117,7 @@ class Problem:
             cmp_ratio=self.cmp_ratio, ori_mask_mode=self.ori_mask_mode, cmp_mask_mode=self.cmp_mask_mode,
             ori_win_left=self.ori_win_left, ori_win_right=self.ori_win_right, layout_q=self.layout_q,
             layout_kv=self.layout_kv, has_ori_kv=1, has_cmp_kv=int(self.has_cmp_kv), dtype=self.dtype,
-            kv_format=1 if self.kv_format == "int8_packed" else 0, ori_block_size=self.ori_block_size,
+            kv_format=KV_FORMAT_CODES[self.kv_format], ori_block_size=self.ori_block_size,
             cmp_block_size=self.cmp_block_size, return_lse=int(self.return_lse))
 
     def tensor_kwargs(self) -> dict:
@@ -148,20 +154,31 @@ def _fill_normal(buf: torch.Tensor, g: torch.Generator, chunk: int = 1 << 27) ->
 
 
 def _fill_packed(buf: torch.Tensor, g: torch.Generator, rope_dtype: torch.dtype, rope_head_dim: int,
-                 chunk_rows: int = 1 << 18) -> None:
-    """Fill packed int8 rows: int8 ~ U[-127,127], rope ~ N(0,1), scales ~ lognormal(0,0.5)/127."""
+                 fp8: bool = False, chunk_rows: int = 1 << 18) -> None:
+    """Fill packed rows.  int8: NoPE ~ U[-127,127], scales ~ lognormal(0,0.5)/127.
+    fp8 (E4M3FN): NoPE = N(0,1) * 32 clamped to the finite range [-448, 448]
+    and rounded to the nearest E4M3 value (codes span the normal and
+    subnormal exponents; no NaN code), scales ~ lognormal(0,0.5)/32.  Rope
+    ~ N(0,1) in the input dtype."""
     rows = buf.view(-1, buf.shape[-1])
     n = rows.shape[0]
     rope_bytes = rope_head_dim * 2
     for s in range(0, n, chunk_rows):
         e = min(n, s + chunk_rows)
         r = e - s
-        nope = torch.randint(-127, 128, (r, 512), generator=g, device=buf.device, dtype=torch.int16)
-        rows[s:e, :512].copy_(nope.to(torch.int8).view(torch.uint8))
+        if fp8:
+            x = torch.randn(r, 512, generator=g, device=buf.device) * 32.0
+            nope = x.clamp_(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8)
+            rows[s:e, :512].copy_(nope)
+            div = 32.0
+        else:
+            nope = torch.randint(-127, 128, (r, 512), generator=g, device=buf.device, dtype=torch.int16)
+            rows[s:e, :512].copy_(nope.to(torch.int8).view(torch.uint8))
+            div = 127.0
         if rope_bytes:
             rope = torch.randn(r, rope_head_dim, generator=g, device=buf.device).to(rope_dtype)
             rows[s:e, 512:512 + rope_bytes].copy_(rope.view(torch.uint8))
-        scales = (torch.randn(r, 4, generator=g, device=buf.device) * 0.5).exp() / 127.0
+        scales = (torch.randn(r, 4, generator=g, device=buf.device) * 0.5).exp() / div
         rows[s:e, 512 + rope_bytes:512 + rope_bytes + 16].copy_(scales.to(torch.float32).view(torch.uint8))
 
 
@@ -248,7 +265,8 @@ def build(name: str, *, seed: int, device="cpu", q_n: int, q_lens: Sequence[int]
     assert len(kv_lens) == B
     g = _gen(seed, device)
     tdt = torch.bfloat16 if dtype == "bf16" else torch.float16
-    packed = kv_format == "int8_packed"
+    assert kv_format in KV_FORMAT_CODES
+    packed = kv_format in PACKED_FORMATS
     d_v = HEAD_DIM
     d_qk = d_v + (rope_head_dim if packed else 0)
     has_cmp = mode in ("csa", "hca")
@@ -310,7 +328,7 @@ def build(name: str, *, seed: int, device="cpu", q_n: int, q_lens: Sequence[int]
             shape = (B, cap, 1)
         raw = torch.empty(nrows, stride_bytes, dtype=torch.uint8, device=device)
         if packed:
-            _fill_packed(raw[:, :row_bytes], g, tdt, rope_head_dim)
+            _fill_packed(raw[:, :row_bytes], g, tdt, rope_head_dim, fp8=kv_format == "fp8_packed")
         else:
             vals = torch.empty(nrows, d_v, dtype=tdt, device=device)
             _fill_normal(vals, g)
@@ -492,10 +510,21 @@ def packed_decode(device="cpu", seed: int = 4, batch: int = 64, kv_len: int = 65
                  softmax_scale=1.0 / math.sqrt(576))
 
 
+def packed_fp8_decode(device="cpu", seed: int = 5, batch: int = 64, kv_len: int = 65536) -> Problem:
+    """The packed decode workload with FLOAT8_E4M3FN NoPE bytes (the A5 rows
+    of the kv_quant guide): same shapes, 656-byte rows, top-2048 indices."""
+    return build("packed_fp8_decode", seed=seed, device=device, q_n=128, q_lens=[1] * batch,
+                 kv_lens=[kv_len] * batch, layout_q="BSND", layout_kv="PAGED", mode="ori_sparse",
+                 ori_topk=2048, ori_mask_mode=3, cmp_mask_mode=0, kv_format="fp8_packed",
+                 rope_head_dim=64, ori_block_size=64, sinks=False, return_lse=True,
+                 softmax_scale=1.0 / math.sqrt(576))
+
+
 WORKLOADS = {
     "swa_decode_tiny": swa_decode_tiny,
     "csa_decode": csa_decode,
     "hca_decode": hca_decode,
     "csa_prefill": csa_prefill,
     "packed_decode": packed_decode,
+    "packed_fp8_decode": packed_fp8_decode,
 }

@@ -30,7 +30,7 @@ LIB_PATH = os.path.join(_HERE, "_build", "libsfm.so")
 
 BSND, TND, PAGED = 0, 1, 2
 BF16, FP16 = 0, 1
-KV_PLAIN, KV_INT8_PACKED = 0, 1
+KV_PLAIN, KV_INT8_PACKED, KV_FP8_PACKED = 0, 1, 2
 _LAYOUTS = {"BSND": BSND, "TND": TND, "PAGED": PAGED, "PA_BBND": PAGED, "PA_BSND": PAGED, "PA_ND": PAGED}
 
 STATUS_BAD_INDEX = 0x01

@@ -2,7 +2,7 @@
 //
 // Covers every configuration the boundary accepts: q_n 1..128, bf16 / fp16,
 // BSND / TND / paged KV with padded rows, window / causal / unmasked ori,
-// CSA / HCA compressed KV, token-wise ori indices and the INT8 packed rows of
+// CSA / HCA compressed KV, token-wise ori indices and the INT8 / FP8 packed rows of
 // the kv_quant_sparse_flash_attention guide (dequantised exactly to fp32 in
 // shared memory: K~[d] = int8[d] * scale[d / 128]).
 //
@@ -98,10 +98,20 @@ __device__ __forceinline__ void load_tile(const KParams &kp, Smem &s, int nrows)
                 const float sc = __ldg(reinterpret_cast<const float *>(rp + 512 + 2 * kp.rope) + (j >> 3));
                 const uint4 v = __ldg(reinterpret_cast<const uint4 *>(rp) + j);
                 const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+                if (kp.kv_fp8) {
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const int8_t x = (int8_t)((w[e >> 2] >> (8 * (e & 3))) & 0xffu);
-                    dst[e] = (float)x * sc;
+                    for (int q = 0; q < 4; ++q) {
+                        float f[4];
+                        e4m3x4_to_f32(w[q], f);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) dst[4 * q + e] = f[e] * sc;
+                    }
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const int8_t x = (int8_t)((w[e >> 2] >> (8 * (e & 3))) & 0xffu);
+                        dst[e] = (float)x * sc;
+                    }
                 }
             } else {
 #pragma unroll

@@ -522,10 +522,12 @@ __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(const KParams 
             return true;
         };
         // packed rows: dequantize this warp's 8 rows of tile p from its raw
-        // stage into bf16 stage p % kStages (int8 x the row's per-128 fp32
-        // scale, rounded once; the 64 rope values are copied as they are)
+        // stage into fp16 stage p % kStages (int8 or E4M3 x the row's
+        // per-128 fp32 scale, rounded once; the 64 rope values converted to
+        // fp16)
         int pend = -1;
         uint32_t pend_vm = 0;
+        const bool fp8 = PK && kp.kv_fp8;
         auto convert = [&](int p, uint32_t vmask, bool last) -> bool {
             if (last) cp_async_wait<0>(); else cp_async_wait<1>();
             __syncwarp();
@@ -540,10 +542,20 @@ __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(const KParams 
                 const float sc = *reinterpret_cast<const float *>(row + 640 + 4 * (lane >> 3));
                 const uint32_t w[4] = {v.x, v.y, v.z, v.w};
                 uint32_t o[8];
+                if (fp8) {
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    o[2 * q] = pack2(i8_to_f32(w[q], 0) * sc, i8_to_f32(w[q], 1) * sc, false);
-                    o[2 * q + 1] = pack2(i8_to_f32(w[q], 2) * sc, i8_to_f32(w[q], 3) * sc, false);
+                    for (int q = 0; q < 4; ++q) {
+                        float f[4];
+                        e4m3x4_to_f32(w[q], f);
+                        o[2 * q] = pack2(f[0] * sc, f[1] * sc, false);
+                        o[2 * q + 1] = pack2(f[2] * sc, f[3] * sc, false);
+                    }
+                } else {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        o[2 * q] = pack2(i8_to_f32(w[q], 0) * sc, i8_to_f32(w[q], 1) * sc, false);
+                        o[2 * q + 1] = pack2(i8_to_f32(w[q], 2) * sc, i8_to_f32(w[q], 3) * sc, false);
+                    }
                 }
                 const uint32_t dst = sb + kv_at(st, lane >> 2);
                 *reinterpret_cast<uint4 *>(base + (dst - sb) + sw128(rr, (lane & 3) * 2)) = make_uint4(o[0], o[1], o[2], o[3]);

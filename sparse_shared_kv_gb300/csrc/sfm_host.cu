@@ -21,9 +21,14 @@ int64_t num_tokens(const sfm_params &p)
     return p.layout_q == SFM_LAYOUT_BSND ? (int64_t)p.batch_size * p.max_seqlen_q : (int64_t)p.total_q;
 }
 
+bool is_packed(const sfm_params &p)
+{
+    return p.kv_format == SFM_KV_INT8_PACKED || p.kv_format == SFM_KV_FP8_PACKED;
+}
+
 int64_t row_bytes(const sfm_params &p)
 {
-    if (p.kv_format == SFM_KV_INT8_PACKED) return 512 + 2 * (int64_t)p.rope_head_dim + 16;
+    if (is_packed(p)) return 512 + 2 * (int64_t)p.rope_head_dim + 16;
     return 2 * (int64_t)p.head_dim;
 }
 
@@ -37,7 +42,7 @@ int validate_params(const sfm_params *pp)
     if (p.dtype != SFM_DTYPE_BF16 && p.dtype != SFM_DTYPE_FP16) return SFM_ERR_INVALID_ARG;
     if (p.kv_format == SFM_KV_PLAIN) {
         if (p.rope_head_dim != 0) return SFM_ERR_INVALID_ARG;
-    } else if (p.kv_format == SFM_KV_INT8_PACKED) {
+    } else if (is_packed(p)) {
         if (p.rope_head_dim != 0 && p.rope_head_dim != 64) return SFM_ERR_INVALID_ARG;
     } else {
         return SFM_ERR_INVALID_ARG;
@@ -79,7 +84,7 @@ bool tc_fits(const sfm_params &p)
 {
     if (p.num_heads_q > 128) return false;
     if (p.kv_format == SFM_KV_PLAIN) return true;
-    return p.kv_format == SFM_KV_INT8_PACKED && p.rope_head_dim == 64;   // 656-byte rows
+    return is_packed(p) && p.rope_head_dim == 64;   // 656-byte rows
 }
 
 // Required length tensors (both calls): 参数组约束 / Paged Attention参数组.
@@ -199,7 +204,7 @@ void fill_common(KParams &kp, const sfm_params &p, const Plan &pl)
     memset(&kp, 0, sizeof(kp));
     kp.q_n = p.num_heads_q;
     kp.d_v = 512;
-    kp.rope = p.kv_format == SFM_KV_INT8_PACKED ? p.rope_head_dim : 0;
+    kp.rope = is_packed(p) ? p.rope_head_dim : 0;
     kp.d_qk = 512 + kp.rope;
     kp.batch = p.batch_size;
     kp.q_s = p.max_seqlen_q;
@@ -211,7 +216,8 @@ void fill_common(KParams &kp, const sfm_params &p, const Plan &pl)
     kp.layout_q = p.layout_q;
     kp.layout_kv = p.layout_kv;
     kp.dtype = p.dtype;
-    kp.packed = p.kv_format == SFM_KV_INT8_PACKED;
+    kp.packed = is_packed(p);
+    kp.kv_fp8 = p.kv_format == SFM_KV_FP8_PACKED;
     kp.ori_bs = p.ori_block_size;
     kp.cmp_bs = p.cmp_block_size;
     kp.q_s_div = make_fastdiv(kp.q_s > 0 ? (uint32_t)kp.q_s : 1u);

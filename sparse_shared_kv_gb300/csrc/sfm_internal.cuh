@@ -9,6 +9,7 @@
 // alignment p = kv_len - q_len + i of its CP切分示例.
 #pragma once
 
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -155,6 +156,7 @@ struct KParams {
     int32_t ori_s, cmp_s;                  // BSND per-batch capacity
     int32_t ori_max, cmp_max;              // paged: declared max lengths (length capacity)
     int32_t layout_q, layout_kv, dtype, packed;
+    int32_t kv_fp8;                        // packed NoPE bytes are FLOAT8_E4M3FN (else int8)
     int32_t ori_bs, cmp_bs, ori_bt_stride, cmp_bt_stride;
     FastDiv ori_bs_div, cmp_bs_div;        // division by the block sizes
     FastDiv q_s_div, ratio_div, split_div; // by q_s, cmp_ratio and split_rows
@@ -202,6 +204,23 @@ struct Tok {
     int32_t lo, hi;        // ori window, inclusive (hi < lo: empty)
     int32_t n_ori, n_cmp;  // attended positions of each source (topk entries or contiguous rows)
 };
+
+// Four FLOAT8_E4M3FN bytes of w (byte 0 first) -> fp32, exactly: the PTX
+// conversion to fp16 pairs is exact (every E4M3 value, subnormals included,
+// is an fp16 value) and fp16 -> fp32 is exact.
+__device__ __forceinline__ void e4m3x4_to_f32(uint32_t w, float (&f)[4])
+{
+    uint32_t lo, hi;
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, l;\n\tcvt.rn.f16x2.e4m3x2 %1, h;\n\t}\n"
+        : "=r"(lo), "=r"(hi) : "r"(w));
+    const __half2 a = *reinterpret_cast<const __half2 *>(&lo), b = *reinterpret_cast<const __half2 *>(&hi);
+    const float2 fa = __half22float2(a), fb = __half22float2(b);
+    f[0] = fa.x;
+    f[1] = fa.y;
+    f[2] = fb.x;
+    f[3] = fb.y;
+}
 
 __device__ __forceinline__ int32_t clamp_len(const KParams &kp, int64_t v, int64_t cap)
 {

@@ -18,8 +18,12 @@ def _rows_f64(prob, which: str) -> np.ndarray:
     x = prob.t[which]
     stride = prob.ori_row_stride if which == "ori_kv" else prob.cmp_row_stride
     raw = x.contiguous().view(torch.uint8).reshape(-1, stride).numpy()
-    if prob.kv_format == "int8_packed":
-        nope = raw[:, :512].view(np.int8).astype(np.float64)
+    if prob.kv_format in ("int8_packed", "fp8_packed"):
+        if prob.kv_format == "fp8_packed":
+            codes = torch.from_numpy(np.ascontiguousarray(raw[:, :512]))
+            nope = codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+        else:
+            nope = raw[:, :512].view(np.int8).astype(np.float64)
         r = prob.rope_head_dim
         scales = np.ascontiguousarray(raw[:, 512 + 2 * r:512 + 2 * r + 16]).view(np.float32).astype(np.float64)
         k = nope * np.repeat(scales, 128, axis=1)

@@ -86,6 +86,12 @@ def _tiny_cases():
     cases.append(("packed_rope0_bsnd_any", dict(q_lens=[2], kv_lens=[33], layout_q="BSND", layout_kv="BSND",
                                                 mode="ori_sparse", ori_topk=10, kv_format="int8_packed",
                                                 rope_head_dim=0, index_mode="any", sinks=True)))
+    cases.append(("packed_fp8_paged", dict(q_lens=[1, 2], kv_lens=[90, 40], layout_q="TND", layout_kv="PAGED",
+                                           mode="ori_sparse", ori_topk=12, kv_format="fp8_packed", rope_head_dim=64,
+                                           ori_block_size=16, sinks=True)))
+    cases.append(("packed_fp8_rope0_bsnd", dict(q_lens=[2], kv_lens=[33], layout_q="BSND", layout_kv="BSND",
+                                                mode="ori_sparse", ori_topk=10, kv_format="fp8_packed",
+                                                rope_head_dim=0, index_mode="any")))
     cases.append(("swa_rowpad_tnd", dict(q_lens=[2, 3], kv_lens=[10, 12], layout_q="TND", layout_kv="TND",
                                          mode="swa", win_left=3, win_right=1, kv_row_pad=48)))
     cases.append(("csa_q_longer_than_kv", dict(q_lens=[6], kv_lens=[4], layout_q="TND", layout_kv="TND",
@@ -316,6 +322,50 @@ def test_packed_pow2_scales_equal_plain_rows():
     rows[:, 512:640] = 0
     deq = rows[:, :512].view(torch.int8).to(torch.float32) * scales.repeat_interleave(128, dim=1)
     plain = S.build("pl", seed=12, q_n=4, q_lens=[1, 1], kv_lens=[80, 50], layout_q="BSND", layout_kv="BSND",
+                    mode="ori_sparse", ori_topk=20, sinks=True)
+    plain.t["ori_kv"] = deq.to(torch.bfloat16).view(pk.t["ori_kv"].shape[:-1] + (512,))
+    assert torch.equal(plain.t["ori_kv"].float().view(-1, 512), deq)      # exact in bf16
+    plain.t["q"] = pk.t["q"][..., :512].contiguous()
+    plain.t["ori_sparse_indices"] = pk.t["ori_sparse_indices"]
+    plain.t["sinks"] = pk.t["sinks"]
+    plain.softmax_scale = pk.softmax_scale
+    Op, lp = oracle.forward(pk)
+    Ol, ll = oracle.forward(plain)
+    np.testing.assert_array_equal(Op, Ol)
+    np.testing.assert_array_equal(lp, ll)
+
+
+def test_e4m3_decoder_matches_library_and_definition():
+    """The oracle's FLOAT8_E4M3FN decoder, all 256 codes, against torch's
+    float8_e4m3fn dtype and against values the format's definition fixes
+    (bias 7, subnormals m * 2^-9, largest finite 448, S.1111.111 = NaN)."""
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    ref = codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = np.array([oracle.dec_e4m3(c) for c in range(256)])
+    nan = np.isnan(ref)
+    assert list(np.nonzero(nan)[0]) == [0x7F, 0xFF]
+    assert np.array_equal(np.isnan(got), nan)
+    np.testing.assert_array_equal(got[~nan], ref[~nan])
+    fixed = {0x00: 0.0, 0x01: 2.0 ** -9, 0x07: 7 * 2.0 ** -9, 0x08: 2.0 ** -6, 0x38: 1.0, 0x3C: 1.5,
+             0x40: 2.0, 0x7E: 448.0, 0xB8: -1.0, 0xFE: -448.0}
+    for c, v in fixed.items():
+        assert oracle.dec_e4m3(c) == v, hex(c)
+    assert math.copysign(1.0, oracle.dec_e4m3(0x80)) == -1.0
+
+
+def test_fp8_pow2_scales_are_exact_products():
+    """An FP8 packed row with power-of-two scales dequantises exactly, so the
+    oracle must equal the plain-row oracle on rows holding those products
+    (bf16 holds every E4M3 value times a power of two in range)."""
+    pk = S.build("pk8", seed=13, q_n=4, q_lens=[1, 1], kv_lens=[80, 50], layout_q="BSND", layout_kv="BSND",
+                 mode="ori_sparse", ori_topk=20, kv_format="fp8_packed", rope_head_dim=64, sinks=True)
+    rows = pk.t["ori_kv"].view(-1, 656)
+    nrows = rows.shape[0]
+    scales = torch.pow(2.0, torch.tensor([-4.0, -6.0, -3.0, -5.0])).to(torch.float32).repeat(nrows, 1)
+    rows[:, 640:656] = scales.view(torch.uint8).view(nrows, 16)
+    rows[:, 512:640] = 0
+    deq = rows[:, :512].contiguous().view(torch.float8_e4m3fn).to(torch.float32) * scales.repeat_interleave(128, dim=1)
+    plain = S.build("pl8", seed=13, q_n=4, q_lens=[1, 1], kv_lens=[80, 50], layout_q="BSND", layout_kv="BSND",
                     mode="ori_sparse", ori_topk=20, sinks=True)
     plain.t["ori_kv"] = deq.to(torch.bfloat16).view(pk.t["ori_kv"].shape[:-1] + (512,))
     assert torch.equal(plain.t["ori_kv"].float().view(-1, 512), deq)      # exact in bf16
