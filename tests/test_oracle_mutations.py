@@ -49,6 +49,12 @@ MUTATIONS = [
     ("value rows taken from the score tail",
      "for (int d = 0; d < P->d_v; ++d) o[d] += w * k[d];",
      "for (int d = 0; d < P->d_v; ++d) o[d] += w * k[d + P->d_qk - P->d_v];"),
+    ("e4m3 exponent bias wrong",
+     "else v = ldexp((double)(m + 8), e - 10);", "else v = ldexp((double)(m + 8), e - 9);"),
+    ("e4m3 subnormals decoded as normals",
+     "if (e == 0) v = ldexp((double)m, -9);", "if (e == 0) v = ldexp((double)(m + 8), -10);"),
+    ("fp8 rows decoded as int8",
+     "if (P->kv_packed == 2)", "if (P->kv_packed == 3)"),
     ("fp16 exponent bias wrong",
      "else v = ldexp((double)(m + 1024), e - 25);", "else v = ldexp((double)(m + 1024), e - 24);"),
 ]
@@ -69,6 +75,8 @@ def _pin_calls():
     for m in ("swa", "hca", "csa"):
         calls.append(lambda m=m: pins.test_layout_equivalence(m))
     calls.append(pins.test_packed_pow2_scales_equal_plain_rows)
+    calls.append(pins.test_e4m3_decoder_matches_library_and_definition)
+    calls.append(pins.test_fp8_pow2_scales_are_exact_products)
     calls.append(pins.test_empty_rows_give_zero_and_neg_inf)
     return calls
 
