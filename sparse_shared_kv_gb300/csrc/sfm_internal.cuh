@@ -129,7 +129,7 @@ __host__ __device__ inline int64_t meta_split_off(int G) { return kHdr + (int64_
 __host__ __device__ inline int64_t meta_cost_off(int G, int T) { return kHdr + (int64_t)G + 1 + (int64_t)T + 1; }
 __host__ __device__ inline int64_t meta_rec_off(int G, int T) { return meta_cost_off(G, T) + (int64_t)T + 1; }
 constexpr int kSrecWords = 16;
-constexpr int kWrecWords = 32;
+constexpr int kWrecWords = 16;
 __host__ __device__ inline int64_t meta_srec_off(int G, int T, int64_t wcap)
 {
     (void)wcap;
@@ -204,6 +204,13 @@ struct Tok {
     int32_t lo, hi;        // ori window, inclusive (hi < lo: empty)
     int32_t n_ori, n_cmp;  // attended positions of each source (topk entries or contiguous rows)
 };
+
+// L2 prefetch of the 128-byte line holding p (an ordinary per-thread
+// instruction; no alignment rule)
+__device__ __forceinline__ void prefetch_line_l2(const void *p)
+{
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
 
 // Four FLOAT8_E4M3FN bytes of w (byte 0 first) -> fp32, exactly: the PTX
 // conversion to fp16 pairs is exact (every E4M3 value, subnormals included,

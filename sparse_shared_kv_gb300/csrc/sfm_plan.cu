@@ -29,6 +29,7 @@ namespace {
 constexpr int kPlanThreads = 512;
 constexpr int kSmemRows = 512;           // rows whose records stay in shared memory
 constexpr int kMaxWorkers = 256;         // persistent workers (one per SM)
+constexpr int kMaxSplits = 2048;         // splits whose row map fits in shared memory
 
 // Exclusive prefix sums of two values per thread over the block: a shuffle
 // scan inside each warp, then one warp scans the 32 warp totals.
@@ -91,6 +92,7 @@ __global__ void __launch_bounds__(kPlanThreads) sfm_plan_kernel(KParams kp)
     __shared__ int32_t s_ws[kMaxWorkers + 1];     // worker c's first unit
     __shared__ int32_t s_wrow[kMaxWorkers];       // the row of that unit
     __shared__ int32_t s_wbeg[kMaxWorkers];       // the row's first split
+    __shared__ int32_t s_owner[kMaxSplits];       // split -> row (flat record writes)
     __shared__ int64_t s_tot[2];                  // splits, modelled cost
     __shared__ int s_overflow;
 
@@ -215,21 +217,27 @@ __global__ void __launch_bounds__(kPlanThreads) sfm_plan_kernel(KParams kp)
     //        the same cost.  The workers whose targets fall in the row and
     //        their units come from three divisions per row and a merge walk.
     constexpr int kHalf = kPlanThreads / 2;
+    // split records go out in step 4 as one coalesced stream when the split
+    // -> row map fits in shared memory; otherwise each row writes its own
+    const bool flat = in_smem && W <= kMaxSplits;
     if (tid < kHalf) {
         for (int t = tid; t < T; t += kHalf) {
             int64_t ns, ucost;
             int size;
             row_shape(t, ns, size, ucost);
+            const int64_t s0 = sp_of(t);
+            if (flat) {
+                for (int64_t j = 0; j < ns; ++j) s_owner[s0 + j] = t;
+                continue;
+            }
             int4 r0, r1;
             rec_of(t, r0, r1);
-            const int64_t s0 = sp_of(t);
             const int4 hd = make_int4(t, (int32_t)s0, (int32_t)ns, size);
             for (int64_t j = 0; j < ns && s0 + j < kp.wcap; ++j) {
                 int4 *d = reinterpret_cast<int4 *>(srec + (s0 + j) * kSrecWords);
                 d[0] = hd;
                 d[1] = r0;
                 d[2] = r1;
-                d[3] = make_int4(0, 0, 0, 0);
             }
         }
         if (tid == 0) sp[T] = (int32_t)(W < INT32_MAX ? W : INT32_MAX);
@@ -283,27 +291,41 @@ __global__ void __launch_bounds__(kPlanThreads) sfm_plan_kernel(KParams kp)
     }
     __syncthreads();
 
-    // 4. per worker: its range and its first unit's row record in one place
-    for (int c = tid; c <= G && c <= kMaxWorkers; c += kPlanThreads) {
-        const int32_t u0 = s_ws[c];
-        ws[c] = u0;
-        if (c == G) break;
-        const int32_t u1 = s_ws[c + 1];
-        int4 *d = reinterpret_cast<int4 *>(wrec + (int64_t)c * kWrecWords);
-        d[0] = make_int4(u0, u1, 0, 0);
-        if (u0 < u1) {
-            const int t = s_wrow[c];
+    // 4. every thread writes consecutive 16-byte words of two flat streams,
+    //    so that a warp's stores are contiguous:
+    //    * the split records, words 0-2 of each 64-byte record (row, first
+    //      split, split count and size; the row's two record words);
+    //    * the worker records, words 0-3 (unit range; the first unit's row
+    //      header and record words).
+    auto row_word = [&](int t, int32_t first, int part) -> int4 {
+        if (part == 0) {
             int64_t ns, ucost;
             int size;
             row_shape(t, ns, size, ucost);
-            int4 r0, r1;
-            rec_of(t, r0, r1);
-            d[1] = make_int4(t, s_wbeg[c], (int32_t)ns, size);
-            d[2] = r0;
-            d[3] = r1;
-            d[4] = make_int4(0, 0, 0, 0);
+            return make_int4(t, first, (int32_t)ns, size);
+        }
+        int4 r0, r1;
+        rec_of(t, r0, r1);
+        return part == 1 ? r0 : r1;
+    };
+    if (flat) {
+        for (int64_t i = tid; i < W * 3; i += kPlanThreads) {
+            const int64_t w = i / 3;
+            const int part = (int)(i - w * 3), t = s_owner[w];
+            reinterpret_cast<int4 *>(srec + w * kSrecWords)[part] = row_word(t, s_sp[t], part);
         }
     }
+    const int GW = G < kMaxWorkers ? G : kMaxWorkers;
+    for (int i = tid; i < GW * 4; i += kPlanThreads) {
+        const int c = i >> 2, part = i & 3;
+        const int32_t u0 = s_ws[c], u1 = s_ws[c + 1];
+        int4 v;
+        if (part == 0) v = make_int4(u0, u1, 0, 0);
+        else if (u0 < u1) v = row_word(s_wrow[c], s_wbeg[c], part - 1);
+        else continue;              // an empty range: the rest of the record is never read
+        reinterpret_cast<int4 *>(wrec + (int64_t)c * kWrecWords)[part] = v;
+    }
+    for (int c = tid; c <= GW; c += kPlanThreads) ws[c] = s_ws[c];
     if (tid == 0) {
         meta[H_MAGIC] = kMetaMagic;
         meta[H_FPRINT] = kp.fingerprint;

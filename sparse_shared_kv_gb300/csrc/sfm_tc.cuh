@@ -149,13 +149,6 @@ __device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes)
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
-// L2 prefetch of the 128-byte line holding p (an ordinary per-thread
-// instruction; no alignment rule)
-__device__ __forceinline__ void prefetch_line_l2(const void *p)
-{
-    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
-}
-
 // Share c of G of a buffer of `bytes` bytes (at most `cap` bytes per share).
 __device__ __forceinline__ void prefetch_share(const void *base, int64_t bytes, int c, int G, int64_t cap)
 {
