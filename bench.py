@@ -174,7 +174,8 @@ def accounting(prob, sfm):
     """Attended rows, algorithmic HBM bytes and FLOPs of one pass over the batch."""
     params = sfm.make_params(**prob.attrs())
     tens = sfm.make_tensors(prob.t["q"], prob.t["ori_kv"], **prob.tensor_kwargs())
-    cap = (prob.ori_topk or (prob.ori_win_left + prob.ori_win_right + 1)) + (prob.cmp_topk or prob.max_seqlen_cmp_kv)
+    cap = ((prob.ori_topk * prob.sparse_block_size) or (prob.ori_win_left + prob.ori_win_right + 1)) + \
+        (prob.cmp_topk or prob.max_seqlen_cmp_kv)
     dev = prob.t["q"].device
     rows = torch.full((prob.num_tokens, cap), -1, dtype=torch.int32, device=dev)
     counts = torch.zeros(prob.num_tokens, dtype=torch.int32, device=dev)

@@ -62,7 +62,7 @@
 extern "C" {
 #endif
 
-#define SFM_ABI_VERSION 1
+#define SFM_ABI_VERSION 2
 
 /* A cudaStream_t, passed as an untyped pointer so this header needs no CUDA headers. */
 typedef void *sfm_stream_t;
@@ -143,6 +143,14 @@ typedef struct sfm_params {
                                   takes up to 128 heads with plain rows, or packed rows
                                   with a 64-value rope part; packed rows are computed
                                   with fp16 operands, bf16 q converted exactly) */
+    int32_t sparse_block_size; /* ori_topk > 0 only: tokens per selected block; 0 or 1 =
+                                  token-wise (each ori_sparse_indices entry is a token),
+                                  2..128 (a power of two, dividing ori_block_size when
+                                  paged) = block-wise: entry e selects tokens
+                                  [e * sparse_block_size, (e + 1) * sparse_block_size),
+                                  each still under the ori mask ([QSFA] / [SFA] 属性参数:
+                                  sparse_block_size; the tokens of a block share the
+                                  selection decision) */
 } sfm_params;
 
 /* Device tensors of one call.  Shapes (row = one KV row of row_stride bytes):

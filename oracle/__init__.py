@@ -60,7 +60,7 @@ class OracleProblem(C.Structure):
         ("ori_bs", C.c_int32), ("cmp_bs", C.c_int32), ("ori_bt_stride", C.c_int32), ("cmp_bt_stride", C.c_int32),
         ("ori_row_stride", C.c_int64), ("cmp_row_stride", C.c_int64),
         ("ori_rows", C.c_int64), ("cmp_rows", C.c_int64),
-        ("ori_topk", C.c_int32), ("cmp_topk", C.c_int32), ("cmp_ratio", C.c_int32),
+        ("ori_topk", C.c_int32), ("cmp_topk", C.c_int32), ("cmp_ratio", C.c_int32), ("ori_sbs", C.c_int32),
         ("ori_mask_mode", C.c_int32), ("cmp_mask_mode", C.c_int32), ("win_left", C.c_int32),
         ("win_right", C.c_int32),
         ("has_ori", C.c_int32), ("has_cmp", C.c_int32), ("has_sinks", C.c_int32),
@@ -158,6 +158,7 @@ class _Bound:
         s.ori_topk = prob.ori_topk
         s.cmp_topk = prob.cmp_topk
         s.cmp_ratio = prob.cmp_ratio
+        s.ori_sbs = getattr(prob, "sparse_block_size", 1)
         s.ori_mask_mode = prob.ori_mask_mode
         s.cmp_mask_mode = prob.cmp_mask_mode
         s.win_left = prob.ori_win_left

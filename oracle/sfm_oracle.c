@@ -23,7 +23,10 @@
  *     ori_win_right).  When ori_topk > 0 the ori source is instead the valid
  *     entries of ori_sparse_indices inside that same set (token-wise sparse
  *     selection of the kv_quant_sparse_flash_attention guide, 属性参数:
- *     sparse_block_size = 1, sparse_mode 0/3).
+ *     sparse_block_size = 1, sparse_mode 0/3); with sparse_block_size > 1
+ *     (block-wise selection, same 属性参数 row: the tokens of a block share
+ *     the decision) entry e selects tokens e*sbs .. e*sbs + sbs - 1, each kept
+ *     only inside that set.
  *   - cmp_kv: slot j is visible iff (j+1)*cmp_ratio <= p_cmp + 1 under
  *     cmp_mask_mode 3 (right-down causal), always under mode 0.  HCA attends
  *     every visible slot; CSA attends the valid entries of cmp_sparse_indices
@@ -68,7 +71,7 @@ typedef struct oracle_problem {
     int32_t ori_bs, cmp_bs, ori_bt_stride, cmp_bt_stride;
     int64_t ori_row_stride, cmp_row_stride;   /* bytes between rows */
     int64_t ori_rows, cmp_rows;               /* rows held by each buffer */
-    int32_t ori_topk, cmp_topk, cmp_ratio;
+    int32_t ori_topk, cmp_topk, cmp_ratio, ori_sbs;
     int32_t ori_mask_mode, cmp_mask_mode, win_left, win_right;
     int32_t has_ori, has_cmp, has_sinks;
     double softmax_scale;
@@ -198,12 +201,18 @@ static int64_t attended(const oracle_problem *P, int t, const tok_info *ti, int3
         int64_t lo, hi;
         ori_bounds(P, ti, &lo, &hi);
         if (P->ori_topk > 0) {
+            /* entry k selects the sbs tokens [e * sbs, (e + 1) * sbs); each
+             * token is then kept only inside the ori mask set */
             const int32_t *row = P->ori_idx + (int64_t)t * P->ori_topk;
+            const int64_t sbs = P->ori_sbs > 1 ? P->ori_sbs : 1;
             for (int k = 0; k < P->ori_topk; ++k) {
-                int64_t e = row[k];
-                if (e < 0 || e >= ti->kv_len || e < lo || e > hi) continue;
-                if (n < cap) { src[n] = 0; pos[n] = (int32_t)e; }
-                ++n;
+                if (row[k] < 0) continue;
+                for (int64_t j = 0; j < sbs; ++j) {
+                    const int64_t e = (int64_t)row[k] * sbs + j;
+                    if (e >= ti->kv_len || e < lo || e > hi) continue;
+                    if (n < cap) { src[n] = 0; pos[n] = (int32_t)e; }
+                    ++n;
+                }
             }
         } else {
             for (int64_t e = lo; e <= hi; ++e) {

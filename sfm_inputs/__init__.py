@@ -77,6 +77,7 @@ class Problem:
     kv_lens: List[int] = field(default_factory=list)
     ori_row_stride: int = 0       # bytes between consecutive KV rows
     cmp_row_stride: int = 0
+    sparse_block_size: int = 1    # tokens per ori_sparse_indices entry (block-wise selection)
 
     # ------------------------------------------------------------------
     @property
@@ -118,7 +119,8 @@ class Problem:
             ori_win_left=self.ori_win_left, ori_win_right=self.ori_win_right, layout_q=self.layout_q,
             layout_kv=self.layout_kv, has_ori_kv=1, has_cmp_kv=int(self.has_cmp_kv), dtype=self.dtype,
             kv_format=KV_FORMAT_CODES[self.kv_format], ori_block_size=self.ori_block_size,
-            cmp_block_size=self.cmp_block_size, return_lse=int(self.return_lse))
+            cmp_block_size=self.cmp_block_size, return_lse=int(self.return_lse),
+            sparse_block_size=self.sparse_block_size)
 
     def tensor_kwargs(self) -> dict:
         """Tensors (plus KV row strides) under the names of the library's sfm_tensors."""
@@ -249,7 +251,7 @@ def build(name: str, *, seed: int, device="cpu", q_n: int, q_lens: Sequence[int]
           kv_capacity: Optional[int] = None, seqused_q: Optional[Sequence[int]] = None,
           pass_seqused_ori: Optional[bool] = None, pass_seqused_cmp: Optional[bool] = None,
           residuals: Optional[Sequence[int]] = None, cmp_lens: Optional[Sequence[int]] = None,
-          index_mode: str = "visible", kv_row_pad: int = 0) -> Problem:
+          index_mode: str = "visible", kv_row_pad: int = 0, sparse_block_size: int = 1) -> Problem:
     """Build a problem.
 
     mode: 'swa' (ori window only), 'csa' (window + top-k compressed),
@@ -259,6 +261,8 @@ def build(name: str, *, seed: int, device="cpu", q_n: int, q_lens: Sequence[int]
           'all_visible' lists every visible slot in order (the form the
           context-parallel example builds); 'any' samples from [0, len).
     kv_row_pad: extra bytes between consecutive KV rows (inter-row padding).
+    sparse_block_size: 'ori_sparse' only; each index selects a block of that
+          many tokens (sampled among the blocks holding a visible token).
     """
     assert layout_q in LAYOUTS_Q and layout_kv in LAYOUTS_KV
     B = len(q_lens)
@@ -424,6 +428,7 @@ def build(name: str, *, seed: int, device="cpu", q_n: int, q_lens: Sequence[int]
                 c.append(kv_lens[b])
             else:
                 c.append(max(0, min(kv_lens[b], p + 1)))
+        c = [-(-x // sparse_block_size) for x in c]          # blocks holding a candidate token
         counts = torch.tensor(c, dtype=torch.int64, device=device)
         idx = sample_sorted_subsets(counts, ori_topk, g)
         if layout_q == "BSND":
@@ -445,7 +450,7 @@ def build(name: str, *, seed: int, device="cpu", q_n: int, q_lens: Sequence[int]
         ori_block_size=ori_block_size if layout_kv == "PAGED" else 0,
         cmp_block_size=cmp_block_size if (layout_kv == "PAGED" and has_cmp) else 0,
         return_lse=return_lse, softmax_scale=float(softmax_scale), seed=seed, t=t,
-        q_lens=q_lens, kv_lens=kv_lens)
+        q_lens=q_lens, kv_lens=kv_lens, sparse_block_size=sparse_block_size)
     p.ori_row_stride = ori_stride
     p.cmp_row_stride = cmp_stride
     return p

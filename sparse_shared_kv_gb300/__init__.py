@@ -46,7 +46,7 @@ class SfmParams(C.Structure):
         "num_heads_q", "num_heads_kv", "head_dim", "rope_head_dim", "batch_size", "max_seqlen_q", "total_q",
         "max_seqlen_ori_kv", "max_seqlen_cmp_kv", "ori_topk", "cmp_topk", "cmp_ratio", "ori_mask_mode",
         "cmp_mask_mode", "ori_win_left", "ori_win_right", "layout_q", "layout_kv", "has_ori_kv", "has_cmp_kv",
-        "dtype", "kv_format", "ori_block_size", "cmp_block_size", "return_lse", "kernel_hint")]
+        "dtype", "kv_format", "ori_block_size", "cmp_block_size", "return_lse", "kernel_hint", "sparse_block_size")]
 
     def as_dict(self):
         return {n: getattr(self, n) for n, _ in self._fields_}
@@ -249,7 +249,7 @@ def make_params(**kw) -> SfmParams:
     defaults = dict(num_heads_kv=1, head_dim=512, rope_head_dim=0, total_q=0, max_seqlen_cmp_kv=0, ori_topk=0,
                     cmp_topk=0, cmp_ratio=1, ori_mask_mode=4, cmp_mask_mode=3, ori_win_left=-1, ori_win_right=-1,
                     layout_q=BSND, layout_kv=BSND, has_ori_kv=1, has_cmp_kv=0, dtype=BF16, kv_format=KV_PLAIN,
-                    ori_block_size=0, cmp_block_size=0, return_lse=0, kernel_hint=0)
+                    ori_block_size=0, cmp_block_size=0, return_lse=0, kernel_hint=0, sparse_block_size=1)
     defaults.update(kw)
     for k, v in defaults.items():
         if k in ("layout_q", "layout_kv") and isinstance(v, str):
@@ -278,7 +278,7 @@ def sparse_flash_mla_metadata(num_heads_q: int, num_heads_kv: int, head_dim: int
                               ori_win_right=-1, layout_q="BSND", layout_kv="BSND", has_ori_kv=True,
                               has_cmp_kv=True, dtype=torch.bfloat16, kv_format=KV_PLAIN, rope_head_dim=0,
                               ori_block_size=0, cmp_block_size=0, return_softmax_lse=False,
-                              device=None, stream=None) -> Metadata:
+                              sparse_block_size=1, device=None, stream=None) -> Metadata:
     """Enqueue the device planner and return its plan (two-call contract)."""
     if layout_q == "TND" and cu_seqlens_q is not None:
         batch_size = cu_seqlens_q.numel() - 1
@@ -289,7 +289,7 @@ def sparse_flash_mla_metadata(num_heads_q: int, num_heads_kv: int, head_dim: int
         ori_mask_mode=ori_mask_mode, cmp_mask_mode=cmp_mask_mode, ori_win_left=ori_win_left,
         ori_win_right=ori_win_right, layout_q=layout_q, layout_kv=layout_kv, has_ori_kv=int(has_ori_kv),
         has_cmp_kv=int(has_cmp_kv), dtype=dtype, kv_format=kv_format, ori_block_size=ori_block_size,
-        cmp_block_size=cmp_block_size, return_lse=int(return_softmax_lse))
+        cmp_block_size=cmp_block_size, return_lse=int(return_softmax_lse), sparse_block_size=sparse_block_size)
     lengths = make_tensors(None, None, cu_seqlens_q=cu_seqlens_q, cu_seqlens_ori_kv=cu_seqlens_ori_kv,
                            cu_seqlens_cmp_kv=cu_seqlens_cmp_kv, seqused_q=seqused_q, seqused_ori_kv=seqused_ori_kv,
                            seqused_cmp_kv=seqused_cmp_kv, cmp_residual_kv=cmp_residual_kv, ori_row_stride=0)

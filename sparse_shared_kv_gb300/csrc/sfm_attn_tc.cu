@@ -242,7 +242,7 @@ __device__ __forceinline__ void resolve_tiles(const KParams &kp, const Unit &s, 
         const bool from_idx = in[j] && (cmp[j] ? kp.cmp_topk > 0 : kp.ori_topk > 0);
         const int32_t *ip = !from_idx ? safe
                             : cmp[j]  ? kp.cmp_idx + (int64_t)s.t * kp.cmp_topk + jj
-                                      : kp.ori_idx + (int64_t)s.t * kp.ori_topk + pos;
+                                      : kp.ori_idx + (int64_t)s.t * kp.ori_topk + (pos >> kp.sbs_log2);
         const int v = __ldg(ip);
         e[j] = from_idx ? v : (cmp[j] ? jj : k.lo + pos);
     }
@@ -251,8 +251,13 @@ __device__ __forceinline__ void resolve_tiles(const KParams &kp, const Unit &s, 
     for (int j = 0; j < K; ++j) {
         bool ok = in[j];
         if (ok && !cmp[j] && kp.ori_topk > 0) {
-            if (e[j] >= k.kv_len) err |= SFM_STATUS_BAD_INDEX;
-            ok = e[j] >= 0 && e[j] < k.kv_len && e[j] >= k.lo && e[j] <= k.hi;
+            // block-wise entries: the block start, then this position's token in it
+            const int pos = s.pos0 + (i0 + j) * NT + lane;
+            const int64_t blk0 = (int64_t)e[j] << kp.sbs_log2;
+            const int64_t tok = blk0 + (pos & ((1 << kp.sbs_log2) - 1));
+            if (e[j] >= 0 && blk0 >= k.kv_len) err |= SFM_STATUS_BAD_INDEX;
+            ok = e[j] >= 0 && tok < k.kv_len && tok >= k.lo && tok <= k.hi;
+            e[j] = ok ? (int)tok : 0;
         } else if (ok && cmp[j] && kp.cmp_topk > 0) {
             if (e[j] >= k.cmp_len) err |= SFM_STATUS_BAD_INDEX;
             ok = e[j] >= 0 && e[j] < k.cmp_len &&

@@ -21,6 +21,9 @@ int64_t num_tokens(const sfm_params &p)
     return p.layout_q == SFM_LAYOUT_BSND ? (int64_t)p.batch_size * p.max_seqlen_q : (int64_t)p.total_q;
 }
 
+// tokens per ori_sparse_indices entry (0 means the token-wise default)
+int sparse_block(const sfm_params &p) { return p.sparse_block_size == 0 ? 1 : p.sparse_block_size; }
+
 bool is_packed(const sfm_params &p)
 {
     return p.kv_format == SFM_KV_INT8_PACKED || p.kv_format == SFM_KV_FP8_PACKED;
@@ -60,6 +63,13 @@ int validate_params(const sfm_params *pp)
     if (p.cmp_mask_mode != 0 && p.cmp_mask_mode != 3) return SFM_ERR_INVALID_ARG;
     if (p.ori_win_left < -1 || p.ori_win_right < -1) return SFM_ERR_INVALID_ARG;
     if (p.ori_topk < 0 || p.cmp_topk < 0) return SFM_ERR_INVALID_ARG;
+    {
+        const int sbs = sparse_block(p);
+        if (sbs < 1 || sbs > 128 || (sbs & (sbs - 1))) return SFM_ERR_INVALID_ARG;
+        if (sbs > 1 && p.ori_topk == 0) return SFM_ERR_INVALID_ARG;
+        if (sbs > 1 && p.layout_kv == SFM_LAYOUT_PAGED && p.ori_block_size % sbs) return SFM_ERR_LAYOUT;
+        if ((int64_t)p.ori_topk * sbs > INT32_MAX) return SFM_ERR_INVALID_ARG;
+    }
     if (p.max_seqlen_ori_kv <= 0) return SFM_ERR_INVALID_ARG;
     if (!p.has_cmp_kv) {
         if (p.cmp_topk != 0 || p.cmp_ratio != 1) return SFM_ERR_INVALID_ARG;    // SWA: cmp_topk 0, cmp_ratio 1
@@ -117,7 +127,7 @@ int64_t max_positions(const sfm_params &p)
 {
     int64_t ori;
     if (p.ori_topk > 0) {
-        ori = p.ori_topk;
+        ori = (int64_t)p.ori_topk * sparse_block(p);
     } else {
         ori = p.max_seqlen_ori_kv;
         if (p.ori_mask_mode == 4 && p.ori_win_left >= 0 && p.ori_win_right >= 0) {
@@ -226,6 +236,11 @@ void fill_common(KParams &kp, const sfm_params &p, const Plan &pl)
     kp.ori_bs_div = make_fastdiv(p.ori_block_size > 0 ? (uint32_t)p.ori_block_size : 1u);
     kp.cmp_bs_div = make_fastdiv(p.cmp_block_size > 0 ? (uint32_t)p.cmp_block_size : 1u);
     kp.ori_topk = p.ori_topk;
+    {
+        int l = 0;
+        while ((1 << l) < sparse_block(p)) ++l;
+        kp.sbs_log2 = l;
+    }
     kp.cmp_topk = p.has_cmp_kv ? p.cmp_topk : 0;
     kp.cmp_ratio = p.cmp_ratio;
     kp.ori_mask_mode = p.ori_mask_mode;

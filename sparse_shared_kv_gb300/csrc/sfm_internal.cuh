@@ -162,6 +162,7 @@ struct KParams {
     FastDiv q_s_div, ratio_div, split_div; // by q_s, cmp_ratio and split_rows
     int64_t ori_row_stride, cmp_row_stride, ori_rows, cmp_rows;
     int32_t ori_topk, cmp_topk, cmp_ratio, ori_mask_mode, cmp_mask_mode, win_left, win_right;
+    int32_t sbs_log2;                      // log2 of the tokens per ori_sparse_indices entry
     int32_t has_cmp, return_lse;
     float scale;                            // softmax_scale
     float scale_log2;                       // softmax_scale * log2(e)
@@ -295,7 +296,7 @@ __device__ inline Tok token_info(const KParams &kp, int t)
 
     k.n_ori = 0;
     k.n_cmp = 0;
-    if (k.valid && k.kv_len > 0) k.n_ori = kp.ori_topk > 0 ? kp.ori_topk : (int32_t)(hi - lo + 1);
+    if (k.valid && k.kv_len > 0) k.n_ori = kp.ori_topk > 0 ? kp.ori_topk << kp.sbs_log2 : (int32_t)(hi - lo + 1);
     if (k.valid && kp.has_cmp && k.cmp_len > 0) {
         if (kp.cmp_topk > 0) {
             k.n_cmp = kp.cmp_topk;
@@ -339,9 +340,12 @@ __device__ inline const uint8_t *resolve_row(const KParams &kp, const Tok &k, in
     if (pos < k.n_ori) {
         s = 0;
         if (kp.ori_topk > 0) {
-            e = __ldg(kp.ori_idx + (int64_t)t * kp.ori_topk + pos);
-            if (e >= k.kv_len) set_status(kp, SFM_STATUS_BAD_INDEX);
-            ok = e >= 0 && e < k.kv_len && e >= k.lo && e <= k.hi;
+            // entry pos >> sbs_log2 selects a block of 2^sbs_log2 tokens
+            const int idx = __ldg(kp.ori_idx + (int64_t)t * kp.ori_topk + (pos >> kp.sbs_log2));
+            const int64_t tok = ((int64_t)idx << kp.sbs_log2) + (pos & ((1 << kp.sbs_log2) - 1));
+            if (idx >= 0 && ((int64_t)idx << kp.sbs_log2) >= k.kv_len) set_status(kp, SFM_STATUS_BAD_INDEX);
+            ok = idx >= 0 && tok < k.kv_len && tok >= k.lo && tok <= k.hi;
+            e = ok ? (int)tok : -1;
         } else {
             e = k.lo + pos;
             ok = true;

@@ -110,9 +110,14 @@ def dense_reference(prob, t: int, rows_cache=None):
             if R >= 0:
                 mask &= pos <= p + R
         if prob.ori_topk > 0:
+            # block-wise selection: a histogram over block ids, spread over the
+            # sbs tokens of each block, then the token mask
+            sbs = max(1, getattr(prob, "sparse_block_size", 1))
+            nblk = -(-kv // sbs)
             idx = prob.t["ori_sparse_indices"].reshape(-1, prob.ori_topk)[t].numpy()
-            idx = idx[(idx >= 0) & (idx < kv)]
-            mult = np.bincount(idx, minlength=kv).astype(np.float64) * mask
+            idx = idx[(idx >= 0) & (idx < nblk)]
+            per_block = np.bincount(idx, minlength=nblk).astype(np.float64)
+            mult = np.repeat(per_block, sbs)[:kv] * mask
         else:
             mult = mask.astype(np.float64)
         S_parts.append(q @ K.T * prob.softmax_scale)

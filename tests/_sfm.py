@@ -60,8 +60,8 @@ def debug_sets(prob, cap=None):
         cap = 1
         for name in ("ori_sparse_indices", "cmp_sparse_indices"):
             x = prob.t[name]
-            if x is not None:
-                cap += x.shape[-1]
+            if x is not None:                       # ori entries select sparse_block_size tokens each
+                cap += x.shape[-1] * (prob.sparse_block_size if name == "ori_sparse_indices" else 1)
         if prob.ori_topk == 0:
             w = prob.max_seqlen_ori_kv
             if prob.ori_mask_mode == 4 and prob.ori_win_left >= 0 and prob.ori_win_right >= 0:

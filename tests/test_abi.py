@@ -32,7 +32,7 @@ def test_header_declares_the_entry_points():
 def test_library_exports_every_declared_symbol(lib):
     for name in declared_functions():
         assert hasattr(lib, name), name
-    assert sfm.sfm_abi_version() == 1
+    assert sfm.sfm_abi_version() == 2
 
 
 def test_error_strings(lib):
@@ -68,6 +68,13 @@ BAD = [
     ("TND without total_q", dict(layout_q=sfm.TND, layout_kv=sfm.TND, total_q=0), 1),
     ("dtype 7", dict(dtype=7), 1),
     ("return_lse 2", dict(return_lse=2), 1),
+    ("fp8 packed rope 32", dict(kv_format=sfm.KV_FP8_PACKED, rope_head_dim=32), 1),
+    ("kv format 3", dict(kv_format=3), 1),
+    ("block-wise without ori_topk", dict(sparse_block_size=4), 1),
+    ("block-wise 3", dict(ori_topk=64, ori_mask_mode=3, sparse_block_size=3), 1),
+    ("block-wise 256", dict(ori_topk=64, ori_mask_mode=3, sparse_block_size=256), 1),
+    ("block-wise not dividing the page", dict(ori_topk=64, ori_mask_mode=3, sparse_block_size=32,
+                                              layout_kv=sfm.PAGED, ori_block_size=16), 3),
 ]
 
 

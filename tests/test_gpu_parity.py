@@ -389,6 +389,23 @@ def test_kernel_paths_prefill_fp16(hint):
     assert_parity(prob, out, lse)
 
 
+@pytest.mark.parametrize("sbs", [2, 16, 64])
+@pytest.mark.parametrize("hint", [1, 2], ids=["cuda_core", "tensor_core"])
+def test_blockwise_selection(sbs, hint):
+    # block-wise top-k over a paged packed pool (each index selects sbs
+    # consecutive tokens, masked per token by right-down causality); indices
+    # include masked (-1), partly visible and out-of-range blocks
+    prob = S.build(f"blockwise{sbs}", seed=400 + sbs, device="cuda", q_n=64, q_lens=[1, 2, 1],
+                   kv_lens=[1500, 3000, 200], layout_q="BSND", layout_kv="PAGED", mode="ori_sparse",
+                   ori_topk=2048 // sbs, ori_mask_mode=3, cmp_mask_mode=0, kv_format="int8_packed",
+                   rope_head_dim=64, ori_block_size=64, sparse_block_size=sbs, index_mode="any",
+                   softmax_scale=1.0 / 24.0)
+    out, lse, status = _sfm.Runner(prob, params=_sfm.params_of(prob, kernel_hint=hint)).run()
+    assert status in (0, 1), hex(status)
+    assert_parity(prob, out, lse)
+    assert_sets(prob)
+
+
 def test_tensor_core_hint_rejects_unsupported():
     # packed rows without the rope part (528 bytes) have no tensor-core path;
     # asking for one is an error

@@ -55,6 +55,10 @@ MUTATIONS = [
      "if (e == 0) v = ldexp((double)m, -9);", "if (e == 0) v = ldexp((double)(m + 8), -10);"),
     ("fp8 rows decoded as int8",
      "if (P->kv_packed == 2)", "if (P->kv_packed == 3)"),
+    ("block-wise selection ignored",
+     "const int64_t sbs = P->ori_sbs > 1 ? P->ori_sbs : 1;", "const int64_t sbs = 1;"),
+    ("block-wise tokens not masked",
+     "if (e >= ti->kv_len || e < lo || e > hi) continue;", "if (e >= ti->kv_len) continue;"),
     ("fp16 exponent bias wrong",
      "else v = ldexp((double)(m + 1024), e - 25);", "else v = ldexp((double)(m + 1024), e - 24);"),
 ]

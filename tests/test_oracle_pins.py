@@ -92,6 +92,13 @@ def _tiny_cases():
     cases.append(("packed_fp8_rope0_bsnd", dict(q_lens=[2], kv_lens=[33], layout_q="BSND", layout_kv="BSND",
                                                 mode="ori_sparse", ori_topk=10, kv_format="fp8_packed",
                                                 rope_head_dim=0, index_mode="any")))
+    cases.append(("packed_blockwise4_paged", dict(q_lens=[1, 2], kv_lens=[90, 45], layout_q="TND",
+                                                  layout_kv="PAGED", mode="ori_sparse", ori_topk=6,
+                                                  kv_format="int8_packed", rope_head_dim=64, ori_block_size=16,
+                                                  sparse_block_size=4, sinks=True)))
+    cases.append(("plain_blockwise16_any", dict(q_lens=[2, 1], kv_lens=[70, 40], layout_q="BSND",
+                                                layout_kv="BSND", mode="ori_sparse", ori_topk=3,
+                                                sparse_block_size=16, index_mode="any")))
     cases.append(("swa_rowpad_tnd", dict(q_lens=[2, 3], kv_lens=[10, 12], layout_q="TND", layout_kv="TND",
                                          mode="swa", win_left=3, win_right=1, kv_row_pad=48)))
     cases.append(("csa_q_longer_than_kv", dict(q_lens=[6], kv_lens=[4], layout_q="TND", layout_kv="TND",
