@@ -139,10 +139,11 @@ typedef struct sfm_params {
     int32_t cmp_block_size;    /* paged with cmp_kv: rows per cmp block, multiple of 16, <= 1024 */
     int32_t return_lse;        /* 1: write LSE (fp32, token-major x q_n) */
     int32_t kernel_hint;       /* 0: automatic; 1: CUDA-core kernel; 2: tensor-core kernel
-                                  (SFM_ERR_UNSUPPORTED when the params do not fit it: it
-                                  takes up to 128 heads with plain rows, or packed rows
-                                  with a 64-value rope part; packed rows are computed
-                                  with fp16 operands, bf16 q converted exactly) */
+                                  (SFM_ERR_UNSUPPORTED when the params do not fit it; it
+                                  takes every supported shape: up to 128 heads, plain or
+                                  packed rows; packed rows are computed with fp16 operands,
+                                  bf16 q converted exactly, and rope-0 packed rows with a
+                                  zero rope block, as if padded) */
     int32_t sparse_block_size; /* ori_topk > 0 only: tokens per selected block; 0 or 1 =
                                   token-wise (each ori_sparse_indices entry is a token),
                                   2..128 (a power of two, dividing ori_block_size when

@@ -394,7 +394,7 @@ __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(const KParams 
             prefetch_share(kp.ori_bt, (int64_t)kp.batch * kp.ori_bt_stride * 4, c, G, kCap);
             if (kp.has_cmp) prefetch_share(kp.cmp_bt, (int64_t)kp.batch * kp.cmp_bt_stride * 4, c, G, kCap);
         }
-        prefetch_share(kp.q, (int64_t)kp.T * kp.q_n * QB * 128, c, G, kCap);
+        prefetch_share(kp.q, (int64_t)kp.T * kp.q_n * kp.d_qk * 2, c, G, kCap);
     }
 
     // everything above overlapped the planner; the plan is read from here on
@@ -485,7 +485,8 @@ __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(const KParams 
         // the unit's Q rows (16 heads per warp); rows past the group's heads are zero
         auto copy_q = [&](const Unit &s) -> bool {
             if (nq > 0 && !warp_wait(bar(B_Q_EMPTY), (nq - 1) & 1, abort_flag)) return false;
-            constexpr int QROW = QB * 128;                  // bytes of one Q head row
+            const int QROW = (int)kp.d_qk * 2;             // bytes of one Q head row in the input
+            const int QC = QROW / 16;                      // its 16-byte chunks (the rest of the QB blocks: zero)
             const uint8_t *qrow = static_cast<const uint8_t *>(kp.q) + ((int64_t)s.t * kp.q_n + s.h0) * QROW;
 #pragma unroll 4
             for (int rr = 0; rr < 64 / kProducers; ++rr) {
@@ -496,7 +497,8 @@ __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(const KParams 
                     const int C = lane + part * 32;
                     if (C < QB * 8) {
                         const uint32_t dst = sb + Q_OFF + (C >> 3) * 8192u + sw128(hh, C & 7);
-                        cp_async16(dst, live ? qrow + (int64_t)hh * QROW + C * 16 : zero_src, live ? 16u : 0u);
+                        const bool in_row = live && C < QC;
+                        cp_async16(dst, in_row ? qrow + (int64_t)hh * QROW + C * 16 : zero_src, in_row ? 16u : 0u);
                     }
                 }
             }
@@ -533,6 +535,11 @@ __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(const KParams 
         int pend = -1;
         uint32_t pend_vm = 0;
         const bool fp8 = PK && kp.kv_fp8;
+        // rope-0 packed rows (528 bytes) keep the 576-dim computation: their
+        // rope operand block is zero in K and in Q, so the products are those
+        // of the same row padded with a zero rope part
+        const bool has_rope = kp.rope > 0;
+        const uint32_t row_bytes = has_rope ? PK_ROW : PK_ROW - 128, scale_off = row_bytes - 16;
         auto convert = [&](int p, uint32_t vmask, bool last) -> bool {
             if (last) cp_async_wait<0>(); else cp_async_wait<1>();
             __syncwarp();
@@ -544,7 +551,7 @@ __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(const KParams 
                 const int rr = pw * kRowsPerWarp + k;
                 const uint8_t *row = rawp + rr * PK_ROW;
                 const uint4 v = *reinterpret_cast<const uint4 *>(row + 16 * lane);   // dims 16 lane .. +15
-                const float sc = *reinterpret_cast<const float *>(row + 640 + 4 * (lane >> 3));
+                const float sc = *reinterpret_cast<const float *>(row + scale_off + 4 * (lane >> 3));
                 const uint32_t w[4] = {v.x, v.y, v.z, v.w};
                 uint32_t o[8];
                 if (fp8) {
@@ -566,9 +573,12 @@ __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(const KParams 
                 *reinterpret_cast<uint4 *>(base + (dst - sb) + sw128(rr, (lane & 3) * 2)) = make_uint4(o[0], o[1], o[2], o[3]);
                 *reinterpret_cast<uint4 *>(base + (dst - sb) + sw128(rr, (lane & 3) * 2 + 1)) =
                     make_uint4(o[4], o[5], o[6], o[7]);
-                if (lane < 8) {                          // rope: input dtype -> fp16
-                    uint4 r4 = *reinterpret_cast<const uint4 *>(row + 512 + 16 * lane);
-                    if (bf16) r4 = bf16x8_to_f16x8(r4);
+                if (lane < 8) {                          // rope: input dtype -> fp16; rope-0 rows: zeros
+                    uint4 r4 = make_uint4(0, 0, 0, 0);
+                    if (has_rope) {
+                        r4 = *reinterpret_cast<const uint4 *>(row + 512 + 16 * lane);
+                        if (bf16) r4 = bf16x8_to_f16x8(r4);
+                    }
                     *reinterpret_cast<uint4 *>(base + kv_at(st, 8) + sw128(rr, lane)) = r4;
                 }
             }
@@ -632,7 +642,7 @@ __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(const KParams 
                         const uint8_t *src = reinterpret_cast<const uint8_t *>(__shfl_sync(0xffffffffu, my_row, rr));
                         const uint32_t dst = raw + rr * PK_ROW;
                         cp_async16(dst + lane * 16, src ? src + lane * 16 : zero_src, src ? 16u : 0u);
-                        if (lane < PK_ROW / 16 - 32)
+                        if (lane < (int)(row_bytes / 16) - 32)
                             cp_async16(dst + (32 + lane) * 16, src ? src + (32 + lane) * 16 : zero_src, src ? 16u : 0u);
                     }
                     cp_async_commit();

@@ -87,14 +87,13 @@ int validate_params(const sfm_params *pp)
     return SFM_OK;
 }
 
-// The tensor-core kernel covers plain bf16 / fp16 rows and packed int8 rows
-// with a 64-value rope part (656 bytes); more than 64 heads run as two work
-// units (head groups) per split.
+// The tensor-core kernel covers plain bf16 / fp16 rows and packed int8 / fp8
+// rows with or without the 64-value rope part (656 / 528 bytes; rope-0 rows
+// run the same 576-dim products with a zero rope block); more than 64 heads
+// run as two work units (head groups) per split.
 bool tc_fits(const sfm_params &p)
 {
-    if (p.num_heads_q > 128) return false;
-    if (p.kv_format == SFM_KV_PLAIN) return true;
-    return is_packed(p) && p.rope_head_dim == 64;   // 656-byte rows
+    return p.kv_format == SFM_KV_PLAIN || is_packed(p);
 }
 
 // Required length tensors (both calls): 参数组约束 / Paged Attention参数组.

@@ -406,25 +406,46 @@ def test_blockwise_selection(sbs, hint):
     assert_sets(prob)
 
 
-def test_tensor_core_hint_rejects_unsupported():
-    # packed rows without the rope part (528 bytes) have no tensor-core path;
-    # asking for one is an error
-    prob = S.build("packed_tc", seed=1, device="cuda", q_n=16, q_lens=[1], kv_lens=[300], layout_q="BSND",
-                   layout_kv="PAGED", mode="ori_sparse", ori_topk=64, ori_mask_mode=3, cmp_mask_mode=0,
-                   kv_format="int8_packed", rope_head_dim=0, ori_block_size=64)
-    with pytest.raises(sfm.SfmError):
-        sfm.sfm_metadata_size(_sfm.params_of(prob, kernel_hint=2))
+@pytest.mark.parametrize("fmt", ["int8_packed", "fp8_packed"])
+def test_rope0_rows_equal_zero_padded_rows(fmt):
+    """Compact 528-byte rows (rope_head_dim 0, q of 512 dims) against the same
+    NoPE bytes and scales in 656-byte rows with a zero rope part and q's rope
+    part zero: bit for bit the same output and LSE on the tensor-core kernel
+    (the kv_quant guide's rope-0 test compares the two with torch.equal)."""
+    kw = dict(seed=77, device="cuda", q_n=64, q_lens=[1, 1], kv_lens=[1200, 700], layout_q="BSND",
+              layout_kv="PAGED", mode="ori_sparse", ori_topk=256, ori_mask_mode=3, cmp_mask_mode=0,
+              kv_format=fmt, ori_block_size=64, sinks=True)
+    p64 = S.build("pad", rope_head_dim=64, **kw)
+    p0 = S.build("compact", rope_head_dim=0, **kw)
+    r64 = p64.t["ori_kv"].view(-1, 656)
+    r0 = p0.t["ori_kv"].view(-1, 528)
+    r64[:, 512:640] = 0                           # zero rope part
+    r64[:, 640:656] = r0[:, 512:528]              # the compact rows' scales
+    r64[:, :512] = r0[:, :512]                    # the compact rows' NoPE bytes
+    p64.t["ori_block_table"] = p0.t["ori_block_table"]
+    p64.t["ori_sparse_indices"] = p0.t["ori_sparse_indices"]
+    p64.t["sinks"] = p0.t["sinks"]
+    q = p64.t["q"]
+    q[..., :512] = p0.t["q"]
+    q[..., 512:] = 0
+    p64.softmax_scale = p0.softmax_scale
+    o64, l64, st64 = _sfm.Runner(p64, params=_sfm.params_of(p64, kernel_hint=2)).run()
+    o0, l0, st0 = _sfm.Runner(p0, params=_sfm.params_of(p0, kernel_hint=2)).run()
+    assert st64 == 0 and st0 == 0
+    assert torch.equal(o64, o0) and torch.equal(l64, l0)
+    assert_parity(p0, o0, l0)
 
 
+@pytest.mark.parametrize("rope", [0, 64])
 @pytest.mark.parametrize("fmt", ["int8_packed", "fp8_packed"])
 @pytest.mark.parametrize("hint", [1, 2], ids=["cuda_core", "tensor_core"])
 @pytest.mark.parametrize("q_n", [16, 64, 128])
-def test_kernel_paths_packed(q_n, hint, fmt):
+def test_kernel_paths_packed(q_n, hint, fmt, rope):
     # packed int8 / E4M3 rows (656 bytes) with token-wise top-k over a paged
     # pool; the index lists include masked (-1) and future entries
     prob = S.build(f"packed{q_n}", seed=300 + q_n, device="cuda", q_n=q_n, q_lens=[1, 1, 1], kv_lens=[900, 3000, 200],
                    layout_q="BSND", layout_kv="PAGED", mode="ori_sparse", ori_topk=256, ori_mask_mode=3,
-                   cmp_mask_mode=0, kv_format=fmt, rope_head_dim=64, ori_block_size=64,
+                   cmp_mask_mode=0, kv_format=fmt, rope_head_dim=rope, ori_block_size=64,
                    index_mode="any", softmax_scale=1.0 / 24.0)
     out, lse, status = _sfm.Runner(prob, params=_sfm.params_of(prob, kernel_hint=hint)).run()
     assert status in (0, 1), hex(status)       # out-of-range indices are flagged (BAD_INDEX) and skipped
