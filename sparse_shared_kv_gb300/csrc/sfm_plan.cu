@@ -101,18 +101,7 @@ __global__ void __launch_bounds__(kPlanThreads) sfm_plan_kernel(KParams kp)
     // dependent of whatever ran before it on the stream (its launch latency
     // overlaps that kernel's tail) and waits for it before reading any input.
     grid_launch_dependents();
-
-    // Two passes over one copy of the code.  The first ("dry") runs before
-    // the dependency wait, while the preceding kernel still works: made-up
-    // lengths, no global read or write, only so that the instruction lines
-    // of the real pass are already in this SM's caches (a cold first pass
-    // costs a few microseconds of instruction fetches on this part).  Only
-    // for plans that fit in shared memory.
-    const bool warm = kp.T <= kSmemRows;
-#pragma unroll 1
-    for (int pass = warm ? 0 : 1; pass < 2; ++pass) {
-    const bool dry = pass == 0;
-    if (!dry) grid_dependency_wait();
+    grid_dependency_wait();
 
     int32_t *meta = kp.meta_w;
     const int T = kp.T, G = kp.G, S = kp.split_rows;
@@ -127,7 +116,7 @@ __global__ void __launch_bounds__(kPlanThreads) sfm_plan_kernel(KParams kp)
     if (tid == 0) {
         s_overflow = G > kMaxWorkers ? 1 : 0;
         s_tot[0] = s_tot[1] = 0;
-        if (!dry) meta[H_LENFLAGS] = 0;       // length problems found while planning are OR-ed here
+        meta[H_LENFLAGS] = 0;       // length problems found while planning are OR-ed here
     }
     __syncthreads();
     kp.status = meta + H_LENFLAGS;
@@ -164,14 +153,7 @@ __global__ void __launch_bounds__(kPlanThreads) sfm_plan_kernel(KParams kp)
 
     // 1. every row once: lengths, window and position counts
     for (int t = tid; t < T; t += kPlanThreads) {
-        Tok k;
-        if (dry) {                        // made up: up to two splits' worth of positions
-            const int f = S < 4096 ? S : 4096;
-            k.b = t; k.kv_len = 2 * f; k.cmp_len = 0; k.p_cmp = 2 * f - 1;
-            k.lo = 0; k.hi = 2 * f - 1; k.n_ori = f; k.n_cmp = f;
-        } else {
-            k = token_info(kp, t);
-        }
+        const Tok k = token_info(kp, t);
         const int4 r0 = make_int4(k.b, k.kv_len, k.cmp_len, k.p_cmp), r1 = make_int4(k.lo, k.hi, k.n_ori, k.n_cmp);
         if (in_smem) {
             s_rec[t][0] = r0;
@@ -203,7 +185,7 @@ __global__ void __launch_bounds__(kPlanThreads) sfm_plan_kernel(KParams kp)
         int size;
         row_shape(t, ns, size, ucost);
         if (ex_s > INT32_MAX || ex_c > INT32_MAX || ns > kp.max_splits) s_overflow = 1;
-        if (!dry) sp[t] = (int32_t)ex_s;
+        sp[t] = (int32_t)ex_s;
         if (in_smem) {
             s_sp[t] = (int32_t)ex_s;
             s_cp[t] = (int32_t)ex_c;
@@ -251,14 +233,14 @@ __global__ void __launch_bounds__(kPlanThreads) sfm_plan_kernel(KParams kp)
             int4 r0, r1;
             rec_of(t, r0, r1);
             const int4 hd = make_int4(t, (int32_t)s0, (int32_t)ns, size);
-            for (int64_t j = 0; j < ns && s0 + j < kp.wcap && !dry; ++j) {
+            for (int64_t j = 0; j < ns && s0 + j < kp.wcap; ++j) {
                 int4 *d = reinterpret_cast<int4 *>(srec + (s0 + j) * kSrecWords);
                 d[0] = hd;
                 d[1] = r0;
                 d[2] = r1;
             }
         }
-        if (tid == 0 && !dry) sp[T] = (int32_t)(W < INT32_MAX ? W : INT32_MAX);
+        if (tid == 0) sp[T] = (int32_t)(W < INT32_MAX ? W : INT32_MAX);
     } else if (total > 0) {
         const bool small = (total + 1) * (G + 1) <= 0xffffffffll;     // boundary arithmetic fits 32 bits
         auto qdiv = [&](int64_t a, int64_t b) -> int64_t {
@@ -331,8 +313,7 @@ __global__ void __launch_bounds__(kPlanThreads) sfm_plan_kernel(KParams kp)
         for (int i = tid; i < W3; i += kPlanThreads) {
             const int w = i / 3;
             const int part = i - w * 3, t = s_owner[w];
-            const int4 v = row_word(t, s_sp[t], part);
-            if (!dry) reinterpret_cast<int4 *>(srec + (int64_t)w * kSrecWords)[part] = v;
+            reinterpret_cast<int4 *>(srec + (int64_t)w * kSrecWords)[part] = row_word(t, s_sp[t], part);
         }
     }
     const int GW = G < kMaxWorkers ? G : kMaxWorkers;
@@ -343,11 +324,10 @@ __global__ void __launch_bounds__(kPlanThreads) sfm_plan_kernel(KParams kp)
         if (part == 0) v = make_int4(u0, u1, 0, 0);
         else if (u0 < u1) v = row_word(s_wrow[c], s_wbeg[c], part - 1);
         else continue;              // an empty range: the rest of the record is never read
-        if (!dry) reinterpret_cast<int4 *>(wrec + (int64_t)c * kWrecWords)[part] = v;
+        reinterpret_cast<int4 *>(wrec + (int64_t)c * kWrecWords)[part] = v;
     }
-    for (int c = tid; c <= GW; c += kPlanThreads)
-        if (!dry) ws[c] = s_ws[c];
-    if (tid == 0 && !dry) {
+    for (int c = tid; c <= GW; c += kPlanThreads) ws[c] = s_ws[c];
+    if (tid == 0) {
         meta[H_MAGIC] = kMetaMagic;
         meta[H_FPRINT] = kp.fingerprint;
         meta[H_TOKENS] = T;
@@ -358,8 +338,6 @@ __global__ void __launch_bounds__(kPlanThreads) sfm_plan_kernel(KParams kp)
         meta[H_FLAGS] = s_overflow ? SFM_STATUS_PLAN_OVERFLOW : 0;
         meta[H_WCAP] = (int32_t)(kp.wcap < INT32_MAX ? kp.wcap : INT32_MAX);
         for (int j = 10; j < kHdr; ++j) meta[j] = 0;
-    }
-    __syncthreads();                      // the real pass starts on settled shared memory
     }
 }
 
