@@ -21,8 +21,9 @@
 //                        gathers sustain about 5 TB/s of random 1 KB rows on
 //                        this part; TMA row gathers (tile::gather4) reach
 //                        about 1.8 TB/s, one-row TMA boxes about 0.7 TB/s;
-//   MMA warps 8, 10      S = Q.K~^T            (M=128, N=32,  K=512)   -> TMEM
-//                        as two independent accumulation chains (K halves);
+//   MMA warps 8, 10      S = Q.K~^T            (M=128, N=32 or 64, K=512 / 576) -> TMEM
+//   (and 11 for packed)  as independent accumulation chains, one per
+//                        issuing warp (two for plain rows, three for packed);
 //   MMA in warp 6        O += P.V~             (M=128, N=256, K=2x32)  -> TMEM
 //                        both products read the SAME staged tile (K-major
 //                        for S, MN-major for P.V); four S buffers, two P
@@ -120,7 +121,8 @@ enum Bar {
     B_ROW_EMPTY = 44,  // [16] the four producer warps took them
     B_TEARDOWN_PV = 60,
     B_TEARDOWN_S2 = 61,
-    kNumBars = 62
+    B_TEARDOWN_S3 = 62,
+    kNumBars = 63
 };
 // offsets inside the misc area
 constexpr uint32_t TMEM_SLOT_REL = 512;
@@ -316,8 +318,13 @@ __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(const KParams 
     // independent accumulation chains of S (TMEM: chain c, stage s at
     // TM_S + 32 (c * kStages + s)); packed rows have two stages, which leaves
     // room for four shorter chains
-    constexpr int kChains = PK ? 4 : 2;
+    constexpr int kChains = PK ? 3 : 2;
+    // S is issued by one warp per chain: the tensor pipe takes products from
+    // several issuing warps at once, while one warp issues one about every
+    // 100-130 ns whatever its size (warps 8 and 10; packed rows also warp 11)
+    constexpr int kIssuers = kChains;
     static_assert(kChains * kStages * NT <= 256, "S buffers fit next to O in TMEM");
+    static_assert((QB * 4) % kChains == 0, "reduction steps split evenly over the chains");
     constexpr uint32_t Q_OFF = L::Q_OFF, P_OFF = L::P_OFF, KV_COL = L::KV_COL, MISC_OFF = L::MISC_OFF;
     constexpr uint32_t EPI_OFF = L::EPI_OFF, TMEM_SLOT_OFF = MISC_OFF + TMEM_SLOT_REL, ABORT_OFF = MISC_OFF + ABORT_REL;
     constexpr uint32_t VALID_OFF = MISC_OFF + VALID_REL, ALPHA_OFF = MISC_OFF + ALPHA_REL;
@@ -351,7 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(const KParams 
         for (int s = 0; s < kStages; ++s) {
             mbar_init(bar(B_KV_FULL + s), PK ? kProducers + 1 : 32 * kProducers + 1);
             mbar_init(bar(B_KV_EMPTY + s), 1);
-            mbar_init(bar(B_S_FULL + s), 2);
+            mbar_init(bar(B_S_FULL + s), kIssuers);
             mbar_init(bar(B_S_FREE + s), 2);
         }
         for (int a = 0; a < 4; ++a) mbar_init(bar(B_ALPHA + a), 2);
@@ -364,11 +371,12 @@ __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(const KParams 
             mbar_init(bar(B_ROW_EMPTY + r), kProducers);
         }
         mbar_init(bar(B_Q_FULL), (PK && kp.dtype == SFM_DTYPE_BF16) ? kProducers : 32 * kProducers);
-        mbar_init(bar(B_Q_EMPTY), 2);
+        mbar_init(bar(B_Q_EMPTY), kIssuers);
         mbar_init(bar(B_STATS), 2);
         mbar_init(bar(B_TEARDOWN), 1);
         mbar_init(bar(B_TEARDOWN_PV), 1);
         mbar_init(bar(B_TEARDOWN_S2), 1);
+        mbar_init(bar(B_TEARDOWN_S3), 1);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -661,18 +669,19 @@ __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(const KParams 
             if (!stop && pend >= 0) convert(pend, pend_vm, true);
         }
         cp_async_wait<0>();
-    } else if (warp == 8 || warp == 10) {
+    } else if (warp == 8 || warp == 10 || (kIssuers > 2 && warp == 11)) {
         // ======================= S issuers =======================
-        // S(i) needs tile i staged and its S buffer free.  Its 32 reduction
-        // steps run as two independent accumulation chains issued by two
-        // warps: warp 8 over dimensions 0..255, warp 10 over 256..511, into
-        // two TMEM halves (chain c, stage st at TM_S + 128 c + 32 st); the
+        // S(i) needs tile i staged and its S buffer free.  Its reduction
+        // steps run as independent accumulation chains, one per issuing warp:
+        // plain rows warps 8 and 10 (dimensions 0..255 and 256..511), packed
+        // rows warps 8, 10 and 11 (192 of the 576 dimensions each), into TMEM
+        // column ranges chain c, stage st at TM_S + 32 (c kStages + st); the
         // softmax adds them.  An even tile and the next tile of the same unit
         // are computed together as one N=64 product, which halves the number
         // of S instructions (the tensor pipe's instruction rate, not its math,
         // bounds these small products).  P.V is issued by warp 6.
         if (lane == 0) {
-            const int c = warp == 8 ? 0 : 1;
+            const int c = warp == 8 ? 0 : warp == 10 ? 1 : 2;     // this warp's chain
             const uint32_t id_s = idesc_f16(128, NT, mma_bf16, false, false);
             const uint32_t id_s2 = idesc_f16(128, 2 * NT, mma_bf16, false, false);
             int g = 0, nq = 0, prev_key = -1;
@@ -705,19 +714,15 @@ __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(const KParams 
                     fence_proxy_async_smem();    // cp.async (generic proxy) writes -> tensor-core reads
                     tc_fence_after();
                     const uint32_t id = nt == 2 ? id_s2 : id_s;
-                    // this warp's kChains / 2 chains, interleaved step by step;
-                    // chain cc covers reduction steps [cc * kSteps, (cc + 1) * kSteps)
+                    // this warp's chain cc = c covers reduction steps
+                    // [cc * kSteps, (cc + 1) * kSteps)
                     constexpr int kSteps = QB * 4 / kChains;
 #pragma unroll 3
                     for (int k = 0; k < kSteps; ++k) {
-#pragma unroll
-                        for (int j = 0; j < kChains / 2; ++j) {
-                            const int cc = c * (kChains / 2) + j;
-                            const uint32_t d = tmem + TM_S + cc * (kStages * NT) + st * NT;
-                            const uint32_t kk = cc * kSteps + k, blk = kk >> 2, sub = (kk & 3) * 32u;
-                            umma_f16(d, sdesc_sw128(sb + Q_OFF + blk * 8192u + sub, 16, 1024),
-                                     sdesc_sw128(sb + kv_at(st, blk) + sub, 16, 1024), id, k > 0);
-                        }
+                        const uint32_t d = tmem + TM_S + c * (kStages * NT) + st * NT;
+                        const uint32_t kk = c * kSteps + k, blk = kk >> 2, sub = (kk & 3) * 32u;
+                        umma_f16(d, sdesc_sw128(sb + Q_OFF + blk * 8192u + sub, 16, 1024),
+                                 sdesc_sw128(sb + kv_at(st, blk) + sub, 16, 1024), id, k > 0);
                     }
                     for (int j = 0; j < nt; ++j) umma_commit(bar(B_S_FULL + st + j));
                     i += nt;
@@ -727,7 +732,7 @@ __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(const KParams 
                 cur = nxt;
             }
             // drain: every MMA this thread issued has completed before TMEM is freed
-            const uint32_t tb = bar(c == 0 ? B_TEARDOWN : B_TEARDOWN_S2);
+            const uint32_t tb = bar(c == 0 ? B_TEARDOWN : c == 1 ? B_TEARDOWN_S2 : B_TEARDOWN_S3);
             umma_commit(tb);
             const uint64_t t0 = globaltimer_ns();
             while (!mbar_try_wait(tb, 0) && globaltimer_ns() - t0 < kTimeoutNs) {
@@ -775,14 +780,13 @@ __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(const KParams 
                             for (int j = 0; j < NT / 2; ++j)
                                 sv[hf * 16 + j] = __float_as_uint(__uint_as_float(sa[j]) + __uint_as_float(sc[j]));
 #pragma unroll
-                            for (int cc = 2; cc < kChains; cc += 2) {
+                            for (int cc = 2; cc < kChains; ++cc) {       // the further chains (packed rows)
                                 tmem_ld16(tmem + lane_base + TM_S + cc * kStages * NT + st * NT + hf * 16, sa);
-                                tmem_ld16(tmem + lane_base + TM_S + (cc + 1) * kStages * NT + st * NT + hf * 16, sc);
                                 tmem_wait_ld();
 #pragma unroll
                                 for (int j = 0; j < NT / 2; ++j)
                                     sv[hf * 16 + j] = __float_as_uint(__uint_as_float(sv[hf * 16 + j]) +
-                                                                      (__uint_as_float(sa[j]) + __uint_as_float(sc[j])));
+                                                                      __uint_as_float(sa[j]));
                             }
                         }
                     }
