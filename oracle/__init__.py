@@ -227,9 +227,9 @@ def dec_e4m3(code: int) -> float:
     return lib().oracle_dec_e4m3(int(code))
 
 
-def token_info(prob, token: int):
+def token_info(prob, token: int, _bound: Optional[_Bound] = None):
     """(b, i, q_len, kv_len, cmp_len, residual, p, p_cmp, in_range)."""
-    b = _Bound(prob)
+    b = _bound or _Bound(prob)
     out = np.zeros(9, dtype=np.int32)
     rc = lib().oracle_token_info(C.byref(b.s), token, out.ctypes.data)
     if rc:

@@ -341,10 +341,170 @@ __global__ void __launch_bounds__(kPlanThreads) sfm_plan_kernel(KParams kp)
     }
 }
 
+// The same plan for a decode batch of at most kSmallRows rows and fewer than
+// kSmallThreads workers, in three short phases and two block barriers:
+//   1. warps 0 and 1 take one row per lane (lengths, window, counts, split
+//      shape) and scan the split counts and modelled costs of their 32 rows
+//      with shuffles;
+//   2. every thread finds, by binary search over the 64 row prefixes, the row
+//      of each split record it writes (one flat stream) and the first unit of
+//      worker c = thread index (the row whose cost span holds c total / G,
+//      then the unit inside it by one division);
+//   3. the worker records go out as one flat stream.
+// No thread runs a serial walk; the general kernel above serves larger batches.
+constexpr int kSmallRows = 64;
+constexpr int kSmallThreads = 256;
+
+__global__ void __launch_bounds__(kSmallThreads) sfm_plan_small_kernel(KParams kp)
+{
+    __shared__ int4 s_r0[kSmallRows], s_r1[kSmallRows];   // the rows' record words
+    __shared__ int2 s_shape[kSmallRows];                   // splits, split size
+    __shared__ int64_t s_is[kSmallRows], s_ic[kSmallRows];  // inclusive split / cost prefix in the row's warp
+    __shared__ int64_t s_wt[2][2];                         // warp totals: splits, cost
+    __shared__ int32_t s_ws[kSmallThreads], s_wrow[kSmallThreads];
+    __shared__ int s_flags[2];
+    __shared__ int s_overflow;
+
+    grid_launch_dependents();
+    grid_dependency_wait();
+
+    int32_t *meta = kp.meta_w;
+    const int T = kp.T, G = kp.G;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int64_t HG = kp.head_groups;
+    int32_t *sp = meta + meta_split_off(G);
+    int32_t *srec = meta + meta_srec_off(G, T, kp.wcap);
+    int32_t *wrec = meta + meta_wrec_off(G, T, kp.wcap);
+
+    // 1. rows
+    if (warp < 2) {
+        if (lane == 0) s_flags[warp] = 0;
+        if (tid == 0) s_overflow = 0;
+        __syncwarp();
+        kp.status = &s_flags[warp];          // length problems of this warp's rows
+        const int t = warp * 32 + lane;
+        int64_t ns = 0, cost = 0;
+        if (t < T) {
+            const Tok k = token_info(kp, t);
+            const int64_t n = (int64_t)k.n_ori + k.n_cmp;
+            ns = num_splits_dev(n, kp.split_div);
+            const int size = split_size_dev(n, kp.split_div);
+            cost = ns * HG * (size + kSplitOverheadRows);
+            s_r0[t] = make_int4(k.b, k.kv_len, k.cmp_len, k.p_cmp);
+            s_r1[t] = make_int4(k.lo, k.hi, k.n_ori, k.n_cmp);
+            s_shape[t] = make_int2((int)ns, size);
+            if (ns > kp.max_splits) s_overflow = 1;
+        }
+        int64_t is = ns, ic = cost;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int64_t us = shfl_up64(is, d), uc = shfl_up64(ic, d);
+            if (lane >= d) {
+                is += us;
+                ic += uc;
+            }
+        }
+        s_is[t] = is;
+        s_ic[t] = ic;
+        if (lane == 31) {
+            s_wt[warp][0] = is;
+            s_wt[warp][1] = ic;
+        }
+    }
+    __syncthreads();
+
+    // row prefixes over the whole batch (rows past T carry no splits and no cost)
+    const int64_t W = T > 32 ? s_wt[0][0] + s_wt[1][0] : s_wt[0][0];
+    const int64_t total = T > 32 ? s_wt[0][1] + s_wt[1][1] : s_wt[0][1];
+    const int64_t units = W * HG;
+    auto incl_s = [&](int t) -> int64_t { return s_is[t] + (t >= 32 ? s_wt[0][0] : 0); };
+    auto incl_c = [&](int t) -> int64_t { return s_ic[t] + (t >= 32 ? s_wt[0][1] : 0); };
+    // the first row whose inclusive prefix passes v (v below the batch total)
+    auto find_row = [&](int64_t v, bool by_cost) -> int {
+        int lo = 0, hi = T - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if ((by_cost ? incl_c(mid) : incl_s(mid)) > v) hi = mid; else lo = mid + 1;
+        }
+        return lo;
+    };
+    auto row_word = [&](int t, int part) -> int4 {
+        if (part == 1) return s_r0[t];
+        if (part == 2) return s_r1[t];
+        const int2 sh = s_shape[t];
+        return make_int4(t, (int32_t)(incl_s(t) - sh.x), sh.x, sh.y);
+    };
+    const bool bad = W > INT32_MAX || units > INT32_MAX || W > kp.wcap || total > INT32_MAX;
+
+    // 2. the split table, the split records (flat), and each worker's first unit
+    if (tid <= T) sp[tid] = tid < T ? (int32_t)(incl_s(tid) - s_shape[tid].x) : (int32_t)(W < INT32_MAX ? W : INT32_MAX);
+    const int64_t WR = (W < kp.wcap ? W : kp.wcap) * 3;
+    if (WR <= INT32_MAX) {                   // 32-bit index arithmetic
+        for (int i = tid; i < (int)WR; i += kSmallThreads) {
+            const int w = i / 3, part = i - w * 3;
+            reinterpret_cast<int4 *>(srec + (int64_t)w * kSrecWords)[part] = row_word(find_row(w, false), part);
+        }
+    } else {
+        for (int64_t i = tid; i < WR; i += kSmallThreads) {
+            const int64_t w = i / 3;
+            const int part = (int)(i - w * 3);
+            reinterpret_cast<int4 *>(srec + w * kSrecWords)[part] = row_word(find_row(w, false), part);
+        }
+    }
+    if (tid <= G) {
+        int32_t u = 0, row = 0;
+        if (tid == G) {
+            u = (int32_t)(units < INT32_MAX ? units : INT32_MAX);
+        } else if (total > 0) {
+            // target(c) = floor(c total / G): the unit whose modelled-cost span holds it
+            const int64_t num = (int64_t)tid * total;
+            const int64_t tgt = (total + 1) * (G + 1) <= 0xffffffffll ? (int64_t)udiv_est((uint32_t)num, (uint32_t)G)
+                                                                     : num / G;
+            row = find_row(tgt, true);
+            const int2 sh = s_shape[row];
+            const int64_t ucost = sh.y + kSplitOverheadRows, nu = (int64_t)sh.x * HG;
+            const int64_t c0 = incl_c(row) - nu * ucost, off = tgt - c0;
+            int64_t j = off <= 0xffffffffll ? (int64_t)udiv_est((uint32_t)off, (uint32_t)ucost) : off / ucost;
+            if (j > nu - 1) j = nu - 1;
+            u = (int32_t)((incl_s(row) - sh.x) * HG + j);
+        }
+        s_ws[tid] = u;
+        s_wrow[tid] = row;
+        meta[meta_ws_off() + tid] = u;
+    }
+    __syncthreads();
+
+    // 3. worker records: the unit range, then the first unit's split record words
+    for (int i = tid; i < G * 4; i += kSmallThreads) {
+        const int c = i >> 2, part = i & 3;
+        const int32_t u0 = s_ws[c], u1 = s_ws[c + 1];
+        int4 v;
+        if (part == 0) v = make_int4(u0, u1, 0, 0);
+        else if (u0 < u1) v = row_word(s_wrow[c], part - 1);
+        else continue;              // an empty range: the rest of the record is never read
+        reinterpret_cast<int4 *>(wrec + (int64_t)c * kWrecWords)[part] = v;
+    }
+    if (tid == 0) {
+        meta[H_MAGIC] = kMetaMagic;
+        meta[H_FPRINT] = kp.fingerprint;
+        meta[H_TOKENS] = T;
+        meta[H_WORKERS] = G;
+        meta[H_SPLIT] = kp.split_rows;
+        meta[H_PATH] = kp.path;
+        meta[H_TOTAL_SPLITS] = (int32_t)(W < INT32_MAX ? W : INT32_MAX);
+        meta[H_FLAGS] = (s_overflow || bad) ? SFM_STATUS_PLAN_OVERFLOW : 0;
+        meta[H_LENFLAGS] = s_flags[0] | s_flags[1];
+        meta[H_WCAP] = (int32_t)(kp.wcap < INT32_MAX ? kp.wcap : INT32_MAX);
+        for (int j = 10; j < kHdr; ++j) meta[j] = 0;
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_plan(const KParams &kp, cudaStream_t st)
 {
+    if (kp.T <= kSmallRows && kp.G < kSmallThreads)
+        return launch_dependent(sfm_plan_small_kernel, dim3(1), dim3(kSmallThreads), (size_t)0, st, kp);
     return launch_dependent(sfm_plan_kernel, dim3(1), dim3(kPlanThreads), (size_t)0, st, kp);
 }
 

@@ -380,6 +380,19 @@ def test_kernel_paths_heads(q_n, hint):
 
 
 @pytest.mark.parametrize("hint", [1, 2], ids=["cuda_core", "tensor_core"])
+def test_many_splits_and_single_split_rows(hint):
+    # a causal decode batch mixing a row of 6000 positions (dozens of splits:
+    # the combine's looped merge past its unrolled case), a row of one split
+    # (written directly by the attention kernel) and rows in between
+    prob = S.build("many_splits", seed=61, device="cuda", q_n=64, q_lens=[1, 1, 1, 1],
+                   kv_lens=[6000, 100, 1300, 2600], layout_q="BSND", layout_kv="PAGED", mode="swa",
+                   ori_mask_mode=3, win_left=-1, win_right=-1, sinks=True)
+    out, lse, status = _sfm.Runner(prob, params=_sfm.params_of(prob, kernel_hint=hint)).run()
+    assert status == 0, hex(status)
+    assert_parity(prob, out, lse)
+
+
+@pytest.mark.parametrize("hint", [1, 2], ids=["cuda_core", "tensor_core"])
 def test_kernel_paths_prefill_fp16(hint):
     prob = S.build("prefill_fp16", seed=23, device="cuda", q_n=64, q_lens=[70, 130], kv_lens=[200, 900],
                    layout_q="TND", layout_kv="PAGED", mode="hca", cmp_ratio=4, dtype="fp16", sinks=True,
