@@ -362,8 +362,8 @@ __global__ void __launch_bounds__(kSmallThreads) sfm_plan_small_kernel(KParams k
     __shared__ int64_t s_is[kSmallRows], s_ic[kSmallRows];  // inclusive split / cost prefix in the row's warp
     __shared__ int64_t s_wt[2][2];                         // warp totals: splits, cost
     __shared__ int32_t s_ws[kSmallThreads], s_wrow[kSmallThreads];
-    __shared__ int s_flags[2];
-    __shared__ int s_overflow;
+    __shared__ int s_flags[2];                             // length problems, per row warp
+    __shared__ int s_over[2];                              // a row with too many splits, per row warp
 
     grid_launch_dependents();
     grid_dependency_wait();
@@ -378,8 +378,10 @@ __global__ void __launch_bounds__(kSmallThreads) sfm_plan_small_kernel(KParams k
 
     // 1. rows
     if (warp < 2) {
-        if (lane == 0) s_flags[warp] = 0;
-        if (tid == 0) s_overflow = 0;
+        if (lane == 0) {
+            s_flags[warp] = 0;
+            s_over[warp] = 0;
+        }
         __syncwarp();
         kp.status = &s_flags[warp];          // length problems of this warp's rows
         const int t = warp * 32 + lane;
@@ -393,7 +395,7 @@ __global__ void __launch_bounds__(kSmallThreads) sfm_plan_small_kernel(KParams k
             s_r0[t] = make_int4(k.b, k.kv_len, k.cmp_len, k.p_cmp);
             s_r1[t] = make_int4(k.lo, k.hi, k.n_ori, k.n_cmp);
             s_shape[t] = make_int2((int)ns, size);
-            if (ns > kp.max_splits) s_overflow = 1;
+            if (ns > kp.max_splits) s_over[warp] = 1;
         }
         int64_t is = ns, ic = cost;
 #pragma unroll
@@ -414,8 +416,8 @@ __global__ void __launch_bounds__(kSmallThreads) sfm_plan_small_kernel(KParams k
     __syncthreads();
 
     // row prefixes over the whole batch (rows past T carry no splits and no cost)
-    const int64_t W = T > 32 ? s_wt[0][0] + s_wt[1][0] : s_wt[0][0];
-    const int64_t total = T > 32 ? s_wt[0][1] + s_wt[1][1] : s_wt[0][1];
+    const int64_t W = s_wt[0][0] + s_wt[1][0];
+    const int64_t total = s_wt[0][1] + s_wt[1][1];
     const int64_t units = W * HG;
     auto incl_s = [&](int t) -> int64_t { return s_is[t] + (t >= 32 ? s_wt[0][0] : 0); };
     auto incl_c = [&](int t) -> int64_t { return s_ic[t] + (t >= 32 ? s_wt[0][1] : 0); };
@@ -434,7 +436,6 @@ __global__ void __launch_bounds__(kSmallThreads) sfm_plan_small_kernel(KParams k
         const int2 sh = s_shape[t];
         return make_int4(t, (int32_t)(incl_s(t) - sh.x), sh.x, sh.y);
     };
-    const bool bad = W > INT32_MAX || units > INT32_MAX || W > kp.wcap || total > INT32_MAX;
 
     // 2. the split table, the split records (flat), and each worker's first unit
     if (tid <= T) sp[tid] = tid < T ? (int32_t)(incl_s(tid) - s_shape[tid].x) : (int32_t)(W < INT32_MAX ? W : INT32_MAX);
@@ -485,6 +486,7 @@ __global__ void __launch_bounds__(kSmallThreads) sfm_plan_small_kernel(KParams k
         reinterpret_cast<int4 *>(wrec + (int64_t)c * kWrecWords)[part] = v;
     }
     if (tid == 0) {
+        const bool bad = W > INT32_MAX || units > INT32_MAX || W > kp.wcap || total > INT32_MAX;
         meta[H_MAGIC] = kMetaMagic;
         meta[H_FPRINT] = kp.fingerprint;
         meta[H_TOKENS] = T;
@@ -492,7 +494,7 @@ __global__ void __launch_bounds__(kSmallThreads) sfm_plan_small_kernel(KParams k
         meta[H_SPLIT] = kp.split_rows;
         meta[H_PATH] = kp.path;
         meta[H_TOTAL_SPLITS] = (int32_t)(W < INT32_MAX ? W : INT32_MAX);
-        meta[H_FLAGS] = (s_overflow || bad) ? SFM_STATUS_PLAN_OVERFLOW : 0;
+        meta[H_FLAGS] = (s_over[0] | s_over[1] | bad) ? SFM_STATUS_PLAN_OVERFLOW : 0;
         meta[H_LENFLAGS] = s_flags[0] | s_flags[1];
         meta[H_WCAP] = (int32_t)(kp.wcap < INT32_MAX ? kp.wcap : INT32_MAX);
         for (int j = 10; j < kHdr; ++j) meta[j] = 0;
