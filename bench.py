@@ -24,7 +24,6 @@ from __future__ import annotations
 
 import argparse
 import hashlib
-import glob
 import json
 import math
 import os
@@ -213,10 +212,15 @@ def accounting(prob, sfm):
             "bt_entries": bt_entries}
 
 
+# the sources the tensor-core attention kernel (the dominant launch of every
+# workload) is compiled from; its traffic figure stays valid while they do
+ATTN_SOURCES = ("sfm_attn_tc.cu", "sfm_tc.cuh", "sfm_internal.cuh")
+
+
 def kernel_source_hash():
     h = hashlib.sha256()
-    for f in sorted(glob.glob(os.path.join(ROOT, "sparse_shared_kv_gb300", "csrc", "*"))):
-        h.update(open(f, "rb").read())
+    for f in ATTN_SOURCES:
+        h.update(open(os.path.join(ROOT, "sparse_shared_kv_gb300", "csrc", f), "rb").read())
     return h.hexdigest()[:16]
 
 
