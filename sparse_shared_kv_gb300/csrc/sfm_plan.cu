@@ -353,7 +353,7 @@ __global__ void __launch_bounds__(kPlanThreads) sfm_plan_kernel(KParams kp)
 //   3. the worker records go out as one flat stream.
 // No thread runs a serial walk; the general kernel above serves larger batches.
 constexpr int kSmallRows = 64;
-constexpr int kSmallThreads = 256;
+constexpr int kSmallThreads = 512;
 
 __global__ void __launch_bounds__(kSmallThreads) sfm_plan_small_kernel(KParams kp)
 {
