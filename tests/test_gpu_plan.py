@@ -136,6 +136,8 @@ CASES = {
     "swa_empty_rows": dict(q_n=16, q_lens=[1] * 6, kv_lens=[0, 500, 0, 1000, 3, 0], layout_kv="PAGED", mode="swa"),
     "causal_many_splits": dict(q_n=64, q_lens=[1, 1, 1, 1], kv_lens=[6000, 100, 1300, 2600], layout_kv="PAGED",
                                mode="swa", ori_mask_mode=3, win_left=-1, win_right=-1),
+    "csa_decode_40_rows": dict(q_n=32, q_lens=[1] * 40, kv_lens=[100 + 211 * b for b in range(40)],
+                               layout_kv="PAGED", mode="csa", cmp_ratio=4, cmp_topk=64),
     "mtp_q2": dict(q_n=32, q_lens=[2, 1, 2], kv_lens=[900, 40, 2500], mode="csa", cmp_ratio=4, cmp_topk=64,
                    seqused_q=[2, 1, 2]),
     # more than 64 rows
