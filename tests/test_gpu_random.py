@@ -1,0 +1,32 @@
+"""GPU parity on seeded random configurations (every mode, layout pair, mask
+mode, dtype, head count, packed format and block-wise selection size the
+parameter rules allow): both attention kernels through the C-ABI against the
+oracle, element by element, and the attended row sets exactly."""
+import pytest
+import torch
+
+import sfm_inputs as S
+import sparse_shared_kv_gb300 as sfm
+from tests import _sfm
+from tests._random_cases import SEEDS, random_case
+from tests.test_gpu_parity import assert_parity, assert_sets
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    sfm.build()
+    torch.cuda.init()
+
+
+@pytest.mark.parametrize("seed", SEEDS)
+def test_random_case_parity(seed):
+    name, q_n, kw = random_case(seed)
+    prob = S.build(name, seed=seed, device="cuda", q_n=q_n, **kw)
+    host = prob.to("cpu")
+    for hint in (1, 2):
+        out, lse, status = _sfm.Runner(prob, params=_sfm.params_of(prob, kernel_hint=hint)).run()
+        assert status == 0, (hint, hex(status))
+        assert_parity(prob, out, lse, host=host)
+    assert_sets(prob, host=host)
