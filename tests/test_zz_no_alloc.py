@@ -52,10 +52,11 @@ def test_noalloc_matches_forward_twice(hint):
 
 def test_noalloc_rejects_oversized_workspace():
     sfm.build()
-    # 128 heads, long HCA rows: the split-KV partials need more than the fixed array
+    # 128 heads, causal rows of up to 131072 positions (dozens of splits per
+    # row): the split-KV partials need more than the fixed array
     p = sfm.make_params(num_heads_q=128, batch_size=256, max_seqlen_q=1, max_seqlen_ori_kv=131072,
-                        max_seqlen_cmp_kv=1024, cmp_ratio=128, ori_mask_mode=4, cmp_mask_mode=3,
-                        ori_win_left=127, ori_win_right=0, layout_q="BSND", layout_kv="PAGED", has_cmp_kv=1,
+                        max_seqlen_cmp_kv=1024, cmp_ratio=128, ori_mask_mode=3, cmp_mask_mode=3,
+                        ori_win_left=-1, ori_win_right=-1, layout_q="BSND", layout_kv="PAGED", has_cmp_kv=1,
                         ori_block_size=128, cmp_block_size=128, return_lse=1)
     assert sfm.sfm_workspace_size(p) > sfm.NOALLOC_WORKSPACE_BYTES
     out = torch.empty(1, dtype=torch.bfloat16, device="cuda")
