@@ -291,6 +291,9 @@ def run_ours(args):
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {int(status.item()):#x} during warm-up")
 
+    # kernels per step: the planner, the attention kernel and, when a row can
+    # have more than one split (a split-KV workspace is needed), the combine
+    launches_per_step = 3 if sfm.sfm_workspace_size(runners[0][1]) > 0 else 2
     K = args.steps
     # the attention kernel is timed on every 4th step: event records between
     # kernels stop the next kernel from overlapping its predecessor (PDL), so
@@ -397,7 +400,8 @@ def run_ours(args):
                 "layout": f"{p0.layout_q}/{p0.layout_kv}", "attended_rows_per_step": rows_per_step,
                 "l2": f"inputs larger than L2: {args.sets} rotating input sets "
                       f"({args.sets * bytes_launch / 1e6:.0f} MB of attended bytes)",
-                "step": "sfm_metadata (device planner) + sfm_forward (attention + combine)",
+                "step": "sfm_metadata (device planner) + sfm_forward (attention"
+                        + (" + split combine)" if launches_per_step == 3 else "; one split per row, no combine)"),
                 "parallelism": f"replicas x{world}",
             },
             "tflops": flops_total / (ms_max * 1e-3) / 1e12,
@@ -414,9 +418,10 @@ def run_ours(args):
                     "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
                     "ms_per_step": e2e_ms / e2e["steps"], "mode": e2e["mode"]},
             "forward_only": {"value": rows_total / (fwd_ms * 1e-3), "unit": "tokens/s", "ms_per_step": fwd_ms / K,
-                             "note": "sfm_forward alone (attention + combine) on plans made beforehand, "
+                             "note": "sfm_forward alone (attention and, when rows have several splits, the "
+                                     "combine) on plans made beforehand, "
                                      "as a model reuses one plan across its layers"},
-            "gpu_launches": 3 * K,
+            "gpu_launches": launches_per_step * K,
             "clocks": clocks,
         }
         print(json.dumps(line))

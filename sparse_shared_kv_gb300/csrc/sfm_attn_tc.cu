@@ -310,6 +310,30 @@ __device__ __forceinline__ void resolve_tiles(const KParams &kp, const Unit &s, 
     if (err) set_status(kp, err);
 }
 
+// Rows without a split, when a plan has at most one split per row and no
+// combine kernel follows the attention kernel: O = 0 and LSE = -inf for every
+// row with no split (every row when the plan was made for other params), and
+// the plan's status, as the combine kernel writes them otherwise.  Rows are
+// spread over the CTAs of the grid.  Kept out of line so the attention
+// kernel's own code and registers do not change with it.
+__device__ __noinline__ void finish_rows_without_split(const int32_t *meta, bool ok, int G, int T, int qn, void *out,
+                                                       float *lse, int32_t *status)
+{
+    const int tid = threadIdx.x;
+    const int32_t *spt = meta + meta_split_off(G);
+    if (blockIdx.x == 0 && tid == 0 && status) {
+        if (!ok) atomicOr(status, SFM_STATUS_METADATA_MISMATCH | meta[H_FLAGS]);
+        else if (meta[H_LENFLAGS]) atomicOr(status, meta[H_LENFLAGS]);
+    }
+    for (int t = blockIdx.x; t < T; t += gridDim.x) {
+        if (ok && spt[t + 1] > spt[t]) continue;          // uniform over the CTA
+        uint4 *o4 = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(out) + (int64_t)t * qn * 512);
+        for (int i = tid; i < qn * 64; i += kThreads) o4[i] = make_uint4(0, 0, 0, 0);
+        if (lse)
+            for (int h = tid; h < qn; h += kThreads) lse[(int64_t)t * qn + h] = -INFINITY;
+    }
+}
+
 template <bool PK>
 __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(const KParams kp)
 {
@@ -1006,6 +1030,12 @@ __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(const KParams 
         }
     }
     __syncwarp();
+
+    if (kp.max_splits <= 1) {
+        // at most one split per row: every row with attended positions was
+        // finished by its unit and no combine kernel follows
+        finish_rows_without_split(kp.meta, meta_ok(kp), kp.G, kp.T, kp.q_n, kp.out, kp.lse, kp.status);
+    }
 
     // ---------------- teardown ----------------
     tc_fence_before();

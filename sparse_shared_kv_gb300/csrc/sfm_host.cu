@@ -433,7 +433,10 @@ int sfm_forward(const sfm_params *params, const sfm_tensors *in, const int32_t *
     const cudaError_t le = pl.path == PATH_TC ? launch_attn_tc(kp, st) : launch_attn_simt(kp, st);
     if (le != cudaSuccess) return SFM_ERR_CUDA;
     if (g_prof_end && cudaEventRecord(g_prof_end, st) != cudaSuccess) return SFM_ERR_CUDA;
-    if (launch_combine(kp, st) != cudaSuccess) return SFM_ERR_CUDA;
+    // at most one split per row: the tensor-core kernel finishes every row
+    // itself (rows without a split included), so there is nothing to merge
+    const bool merge = pl.path != PATH_TC || pl.max_splits_per_token > 1;
+    if (merge && launch_combine(kp, st) != cudaSuccess) return SFM_ERR_CUDA;
     return SFM_OK;
 }
 

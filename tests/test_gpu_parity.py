@@ -276,6 +276,26 @@ def test_metadata_mismatch_zeroes_outputs():
     assert torch.count_nonzero(r.out.float()) == 0 and torch.isneginf(r.lse).all()
 
 
+def test_metadata_mismatch_zeroes_outputs_without_combine():
+    # 128 heads: one split per row, so no combine kernel runs and the
+    # attention kernel itself reports the mismatch and zeroes every row
+    prob = S.build("mismatch128", seed=5, device="cuda", q_n=128, q_lens=[1, 1, 1], kv_lens=[700, 0, 1500],
+                   layout_kv="PAGED", mode="hca", cmp_ratio=128, sinks=True)
+    r = _sfm.Runner(prob)
+    assert sfm.sfm_workspace_size(r.params) == 0
+    out, lse, status = r.run()
+    assert status == 0
+    assert_parity(prob, out, lse)          # the empty row: O = 0, LSE = -inf
+    other = _sfm.params_of(prob, ori_win_left=63)
+    md = torch.empty(sfm.sfm_metadata_size(other), dtype=torch.int32, device="cuda")
+    sfm.sfm_metadata(other, r.tensors, md)
+    r.status.zero_()
+    sfm.sfm_forward(r.params, r.tensors, md, prob.softmax_scale, r.out, r.lse, r.ws, r.status)
+    torch.cuda.synchronize()
+    assert int(r.status.item()) & sfm.STATUS_METADATA_MISMATCH
+    assert torch.count_nonzero(r.out.float()) == 0 and torch.isneginf(r.lse).all()
+
+
 def test_public_two_call_api():
     prob = S.csa_decode(device="cuda", batch=3)
     T = prob.t
