@@ -75,6 +75,11 @@ BAD = [
     ("block-wise 256", dict(ori_topk=64, ori_mask_mode=3, sparse_block_size=256), 1),
     ("block-wise not dividing the page", dict(ori_topk=64, ori_mask_mode=3, sparse_block_size=32,
                                               layout_kv=sfm.PAGED, ori_block_size=16), 3),
+    ("kernel hint 3", dict(kernel_hint=3), 1),
+    ("kernel hint -1", dict(kernel_hint=-1), 1),
+    ("window right -2", dict(ori_win_right=-2), 1),
+    ("paged cmp block 8", dict(layout_kv=sfm.PAGED, ori_block_size=128, has_cmp_kv=1, cmp_ratio=4, cmp_topk=64,
+                               cmp_mask_mode=3, cmp_block_size=8), 3),
 ]
 
 
