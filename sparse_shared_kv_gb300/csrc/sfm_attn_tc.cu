@@ -373,7 +373,7 @@ __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(const KParams 
     // tolerance where bf16 (8-bit) does not; bf16 Q is converted exactly
     // (magnitudes up to 65504).
     const bool mma_bf16 = PK ? false : bf16;
-    grid_launch_dependents();    // the combine kernel may launch; it waits for this grid
+    grid_launch_dependents();    // the next kernel (the combine, or the next planner) may launch; it waits for this grid
 
     // ---------------- set-up ----------------
     for (uint32_t i = tid; i < 24576u / 16u; i += kThreads)

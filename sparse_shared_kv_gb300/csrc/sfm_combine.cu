@@ -12,7 +12,9 @@
 //
 // This kernel also writes the rows no split covers (empty attended set or a
 // query row beyond seqused_q: O = 0, LSE = -inf) and, when the plan does not
-// match the params, zeroes every output and flags the status word.
+// match the params, zeroes every output and flags the status word.  It runs
+// only when a row can have more than one split: for tensor-core plans of at
+// most one split per row the attention kernel finishes every row itself.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <math.h>
