@@ -62,7 +62,7 @@
 extern "C" {
 #endif
 
-#define SFM_ABI_VERSION 2
+#define SFM_ABI_VERSION 3
 
 /* A cudaStream_t, passed as an untyped pointer so this header needs no CUDA headers. */
 typedef void *sfm_stream_t;
@@ -138,12 +138,11 @@ typedef struct sfm_params {
     int32_t ori_block_size;    /* paged: rows per ori block, multiple of 16, <= 1024 */
     int32_t cmp_block_size;    /* paged with cmp_kv: rows per cmp block, multiple of 16, <= 1024 */
     int32_t return_lse;        /* 1: write LSE (fp32, token-major x q_n) */
-    int32_t kernel_hint;       /* 0: automatic; 1: CUDA-core kernel; 2: tensor-core kernel
-                                  (SFM_ERR_UNSUPPORTED when the params do not fit it; it
-                                  takes every supported shape: up to 128 heads, plain or
-                                  packed rows; packed rows are computed with fp16 operands,
-                                  bf16 q converted exactly, and rope-0 packed rows with a
-                                  zero rope block, as if padded) */
+    int32_t kernel_hint;       /* 0 or 2: the tensor-core kernel, which takes every supported
+                                  shape (up to 128 heads, plain or packed rows; packed rows
+                                  are computed with fp16 operands, bf16 q converted exactly,
+                                  and rope-0 packed rows with a zero rope block, as if
+                                  padded); 1 (the former CUDA-core kernel): SFM_ERR_UNSUPPORTED */
     int32_t sparse_block_size; /* ori_topk > 0 only: tokens per selected block; 0 or 1 =
                                   token-wise (each ori_sparse_indices entry is a token),
                                   2..128 (a power of two, dividing ori_block_size when
@@ -168,8 +167,9 @@ typedef struct sfm_params {
  *   sinks                (q_n) fp32 or NULL
  * Row strides are in bytes, >= the row size and a multiple of 16 (rows may be
  * padded between rows, 公共参数组); *_rows is the number of rows
- * the buffer holds (used to bounds-check every resolved row).  Base pointers
- * must be 16-byte aligned. */
+ * the buffer holds (used to bounds-check every resolved row; at most
+ * 2^31 - 2, SFM_ERR_UNSUPPORTED above).  Base pointers must be 16-byte
+ * aligned. */
 typedef struct sfm_tensors {
     const void *q;
     const void *ori_kv;
@@ -245,9 +245,11 @@ int sfm_forward(const sfm_params *params, const sfm_tensors *inputs, const int32
  * passes the inputs, the metadata, out, lse and status.
  *   - Returns SFM_ERR_WORKSPACE, enqueuing nothing, when these params need
  *     more than SFM_NOALLOC_WORKSPACE_BYTES of workspace.
- *   - The first call that needs scratch on a device looks up the array's
- *     device address (cudaGetSymbolAddress) once for that device; make that
- *     first call before any stream capture.
+ *   - Each call that needs scratch looks up the array's device address on
+ *     the current device (cudaGetSymbolAddress, which allocates nothing); the
+ *     first such call on a device loads the module, so make it before any
+ *     stream capture.  The address is not cached, so calls made after a
+ *     device reset use the array of the re-loaded module.
  *   - All calls on a device share the array and it keeps the last call's
  *     contents: calls whose kernels may overlap on the GPU (unordered
  *     streams) race on it.  Every scratch word is written before it is read
@@ -256,14 +258,25 @@ int sfm_forward_noalloc(const sfm_params *params, const sfm_tensors *inputs, con
                         size_t metadata_n, float softmax_scale, void *out, float *lse, int32_t *status,
                         sfm_stream_t stream);
 
-/* Test hook: the rows the kernels resolve for every query row.  For token t
- * and attended position k < counts[t] (ori positions first, then cmp),
- * rows[t * cap + k] = -1 for a skipped entry, else the logical index
- * (ori position, or cmp slot | 0x40000000).  cap >= max positions per row
- * (ori_topk or window size, plus cmp_topk or visible slots); longer rows are
- * truncated and flagged SFM_STATUS_BAD_LENGTH. */
-int sfm_debug_attended(const sfm_params *params, const sfm_tensors *inputs, int32_t *rows, int64_t cap,
-                       int32_t *counts, int32_t *status, sfm_stream_t stream);
+/* Test hook: sfm_forward() (same arguments, same kernels, same outputs)
+ * that also records every KV row the attention kernel's resolver hands to
+ * its copy warps, so the attended sets of the kernel that computes O can be
+ * compared exactly with a reference.  For query row t and attended position
+ * k (ori positions first, then cmp, in index order; k < cap):
+ *   rows[t * cap + k] = -1                       the entry is skipped (masked,
+ *                                                 invalid or out of range),
+ *                     = r (>= 0)                 row r of the ori_kv buffer,
+ *                     = (int32_t)(r | 1u << 31)  row r of the cmp_kv buffer,
+ * where r counts rows of row_stride bytes from the buffer's base (for PAGED
+ * caches: block id * block_size + offset, after the block table).
+ * counts[t] = attended positions of row t (clamped to cap); rows with no
+ * position and entries at k >= counts[t] are left as the caller filled them
+ * (fill counts with 0).  Positions at or beyond cap are not recorded and set
+ * SFM_STATUS_BAD_LENGTH.  rows / counts: device int32, caller-owned. */
+int sfm_debug_attended(const sfm_params *params, const sfm_tensors *inputs, const int32_t *metadata,
+                       size_t metadata_n, float softmax_scale, void *out, float *lse, void *workspace,
+                       size_t workspace_bytes, int32_t *rows, int64_t cap, int32_t *counts, int32_t *status,
+                       sfm_stream_t stream);
 
 /* Optional instrumentation for benchmarks: with both handles non-NULL (two
  * cudaEvent_t of the current device), every following sfm_forward() records

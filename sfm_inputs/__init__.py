@@ -473,13 +473,14 @@ def swa_decode_tiny(device="cpu", seed: int = 0) -> Problem:
                  ori_mask_mode=4, cmp_mask_mode=0, sinks=False, return_lse=True)
 
 
-def csa_decode(device="cpu", seed: int = 1, batch: int = 32) -> Problem:
+def csa_decode(device="cpu", seed: int = 1, batch: int = 32, cmp_topk: int = 512) -> Problem:
     """CSA decode: q_n=64, paged ori (block 128, random permutation),
-    kv_len ~ U[4096, 32768], window 127/0, cmp_ratio 4 paged, top-512
-    visible compressed slots per query, fp32 sinks."""
+    kv_len ~ U[4096, 32768], window 127/0, cmp_ratio 4 paged, top-512 (or
+    top-1024, the other size the pages allow) visible compressed slots per
+    query, fp32 sinks."""
     kv = _uniform_ints(4096, 32768, batch, seed * 7919 + 11)
     return build("csa_decode", seed=seed, device=device, q_n=64, q_lens=[1] * batch, kv_lens=kv,
-                 layout_q="BSND", layout_kv="PAGED", mode="csa", cmp_ratio=4, cmp_topk=512,
+                 layout_q="BSND", layout_kv="PAGED", mode="csa", cmp_ratio=4, cmp_topk=cmp_topk,
                  win_left=127, win_right=0, sinks=True, return_lse=True)
 
 

@@ -92,7 +92,9 @@ def lib():
                                   C.c_size_t, C.c_void_p, C.c_void_p]
         l.sfm_forward_noalloc.argtypes = [P, T, C.c_void_p, C.c_size_t, C.c_float, C.c_void_p, C.c_void_p,
                                           C.c_void_p, C.c_void_p]
-        l.sfm_debug_attended.argtypes = [P, T, C.c_void_p, C.c_int64, C.c_void_p, C.c_void_p, C.c_void_p]
+        l.sfm_debug_attended.argtypes = [P, T, C.c_void_p, C.c_size_t, C.c_float, C.c_void_p, C.c_void_p,
+                                         C.c_void_p, C.c_size_t, C.c_void_p, C.c_int64, C.c_void_p, C.c_void_p,
+                                         C.c_void_p]
         l.sfm_set_profile_events.argtypes = [C.c_void_p, C.c_void_p]
         l.sfm_error_string.argtypes = [C.c_int]
         l.sfm_error_string.restype = C.c_char_p
@@ -184,11 +186,18 @@ def sfm_forward_noalloc(params: SfmParams, tensors: SfmTensors, metadata: torch.
         out.data_ptr(), _ptr(lse), _ptr(status), _stream(stream)))
 
 
-def sfm_debug_attended(params: SfmParams, tensors: SfmTensors, rows: torch.Tensor, cap: int,
-                       counts: torch.Tensor, status: Optional[torch.Tensor] = None, stream=None) -> None:
+def sfm_debug_attended(params: SfmParams, tensors: SfmTensors, metadata: torch.Tensor, softmax_scale: float,
+                       out: torch.Tensor, lse: Optional[torch.Tensor], workspace: Optional[torch.Tensor],
+                       rows: torch.Tensor, cap: int, counts: torch.Tensor, status: Optional[torch.Tensor] = None,
+                       stream=None) -> None:
+    """sfm_forward that also records the KV rows the attention kernel's
+    resolver hands to its copy warps (rows[t * cap + k], see include/sfm.h)."""
+    assert rows.dtype == torch.int32 and counts.dtype == torch.int32
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     _check("sfm_debug_attended", lib().sfm_debug_attended(
-        C.byref(params), C.byref(tensors), rows.data_ptr(), cap, counts.data_ptr(), _ptr(status),
-        _stream(stream)))
+        C.byref(params), C.byref(tensors), metadata.data_ptr(), metadata.numel(), C.c_float(softmax_scale),
+        out.data_ptr(), _ptr(lse), _ptr(workspace), ws_bytes, rows.data_ptr(), cap, counts.data_ptr(),
+        _ptr(status), _stream(stream)))
 
 
 # ---------------------------------------------------------------------------

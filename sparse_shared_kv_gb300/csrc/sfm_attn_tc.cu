@@ -223,7 +223,8 @@ __device__ __forceinline__ uint32_t pack2(float a, float b, bool bf16)
 
 // Row entries of this lane's row in tiles i0 .. i0+K-1 of the unit: -1 for a
 // skipped or masked position, else the pool row with bit 31 set for the
-// compressed pool.  Same rules and status bits as resolve_row().  Every load
+// compressed pool; out-of-range indices (BAD_INDEX) and rows outside the
+// cache (BAD_BLOCK) are skipped and flagged in the status word.  Every load
 // is unconditional, from the real address or from an always-valid one, so
 // that the K index loads and then the K block-table loads each go out back to
 // back: a batch costs two memory round trips whatever K is.
@@ -460,6 +461,19 @@ __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(const KParams 
             // into L2: those tiles wait for a stage to drain before their
             // copies start, and then hit L2
             auto publish = [&](int i0, int K, const int32_t *ent) {
+                if (kp.dbg_rows) {
+                    // attended-row dump: the entries exactly as the copy warps
+                    // will consume them, at the row's attended position
+                    for (int j = 0; j < K; ++j) {
+                        const int pos = s.pos0 + (i0 + j) * NT + lane;
+                        if (pos < s.pos1) {
+                            if (pos < kp.dbg_cap) kp.dbg_rows[(int64_t)s.t * kp.dbg_cap + pos] = ent[j];
+                            else set_status(kp, SFM_STATUS_BAD_LENGTH);
+                        }
+                    }
+                    if (i0 == 0 && s.w == 0 && s.h0 == 0 && lane == 0)
+                        kp.dbg_counts[s.t] = (int32_t)min((int64_t)(s.k.n_ori + s.k.n_cmp), kp.dbg_cap);
+                }
                 for (int j = 0; j < K; ++j) {
                     const int i = i0 + j;
                     if (i >= s.ntiles) break;

@@ -156,23 +156,6 @@ __global__ void __launch_bounds__(kThreads) sfm_combine_kernel(KParams kp)
     }
 }
 
-__global__ void __launch_bounds__(256) sfm_debug_kernel(KParams kp)
-{
-    for (int t = blockIdx.x; t < kp.T; t += gridDim.x) {
-        const Tok k = token_info(kp, t);
-        const int n = k.n_ori + k.n_cmp;
-        if (threadIdx.x == 0) kp.dbg_counts[t] = (int32_t)min((int64_t)n, kp.dbg_cap);
-        if (n > kp.dbg_cap && threadIdx.x == 0) set_status(kp, SFM_STATUS_BAD_LENGTH);
-        for (int pos = threadIdx.x; pos < n && pos < kp.dbg_cap; pos += blockDim.x) {
-            int logical, src;
-            const uint8_t *rp = resolve_row(kp, k, t, pos, &logical, &src);
-            int32_t v = -1;
-            if (rp) v = src ? (logical | 0x40000000) : logical;
-            kp.dbg_rows[(int64_t)t * kp.dbg_cap + pos] = v;
-        }
-    }
-}
-
 }  // namespace
 
 cudaError_t launch_combine(const KParams &kp, cudaStream_t st)
@@ -182,11 +165,5 @@ cudaError_t launch_combine(const KParams &kp, cudaStream_t st)
     return launch_dependent(sfm_combine_kernel, grid, dim3(kThreads), (size_t)0, st, kp);
 }
 
-cudaError_t launch_debug(const KParams &kp, cudaStream_t st)
-{
-    const int grid = kp.T < 4096 ? (kp.T > 0 ? kp.T : 1) : 4096;
-    sfm_debug_kernel<<<grid, 256, 0, st>>>(kp);
-    return cudaGetLastError();
-}
 
 }  // namespace sfm

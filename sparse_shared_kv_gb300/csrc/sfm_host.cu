@@ -16,6 +16,8 @@ namespace {
 
 inline bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
+constexpr int64_t kMaxPoolRows = ((int64_t)1 << 31) - 2;
+
 int64_t num_tokens(const sfm_params &p)
 {
     return p.layout_q == SFM_LAYOUT_BSND ? (int64_t)p.batch_size * p.max_seqlen_q : (int64_t)p.total_q;
@@ -84,16 +86,8 @@ int validate_params(const sfm_params *pp)
     }
     if (p.return_lse != 0 && p.return_lse != 1) return SFM_ERR_INVALID_ARG;
     if (p.kernel_hint < 0 || p.kernel_hint > 2) return SFM_ERR_INVALID_ARG;
+    if (p.kernel_hint == 1) return SFM_ERR_UNSUPPORTED;   // the CUDA-core kernel is retired
     return SFM_OK;
-}
-
-// The tensor-core kernel covers plain bf16 / fp16 rows and packed int8 / fp8
-// rows with or without the 64-value rope part (656 / 528 bytes; rope-0 rows
-// run the same 576-dim products with a zero rope block); more than 64 heads
-// run as two work units (head groups) per split.
-bool tc_fits(const sfm_params &p)
-{
-    return p.kv_format == SFM_KV_PLAIN || is_packed(p);
 }
 
 // Required length tensors (both calls): 参数组约束 / Paged Attention参数组.
@@ -153,12 +147,14 @@ int make_plan(const sfm_params &p, Plan *pl)
     int sms = 0;
     int rc = num_sms(&sms);
     if (rc) return rc;
-    if (p.kernel_hint == 2 && !tc_fits(p)) return SFM_ERR_UNSUPPORTED;
-    pl->path = (p.kernel_hint == 1 || !tc_fits(p)) ? PATH_SIMT : PATH_TC;
-    // The tensor-core kernel keeps one CTA per SM and leaves one SM to the
-    // planner kernel that runs just before it (the attention kernel's set-up
-    // overlaps the planner; a CTA placed on the planner's SM would start late).
-    pl->G = pl->path == PATH_TC && sms > 1 ? sms - 1 : sms;
+    // One attention kernel (tensor cores) covers every supported shape: plain
+    // bf16 / fp16 rows and packed int8 / fp8 rows with or without the rope
+    // part; more than 64 heads run as two work units (head groups) per split.
+    pl->path = PATH_TC;
+    // The kernel keeps one CTA per SM and leaves one SM to the planner kernel
+    // that runs just before it (the attention kernel's set-up overlaps the
+    // planner; a CTA placed on the planner's SM would start late).
+    pl->G = sms > 1 ? sms - 1 : sms;
     pl->T = num_tokens(p);
     const bool decode_like = p.max_seqlen_q <= 16;
     // Tensor-core tiles are 32 rows.  The split size is a constant of the
@@ -170,8 +166,7 @@ int make_plan(const sfm_params &p, Plan *pl)
     // 128 units, no partials to merge).  Measured on one GPU against
     // 768-row splits: HCA decode step -13 %, packed decode -8 %.  Batches of
     // fewer rows leave SMs idle.
-    int split = 256;
-    if (pl->path == PATH_TC) split = p.num_heads_q > 64 ? 2048 : 160;
+    const int split = p.num_heads_q > 64 ? 2048 : 160;
     pl->split_rows = decode_like ? split : (1 << 30);
     const int64_t mp = max_positions(p);
     pl->max_splits_per_token = decode_like ? (mp + pl->split_rows - 1) / pl->split_rows : 1;
@@ -202,10 +197,7 @@ size_t ws_lse_offset(const sfm_params &p, int64_t cap)
     return (o + 255) & ~(size_t)255;
 }
 
-int head_groups(const sfm_params &p, const Plan &pl)
-{
-    return pl.path == PATH_TC ? (p.num_heads_q + 63) / 64 : 1;
-}
+int head_groups(const sfm_params &p) { return (p.num_heads_q + 63) / 64; }
 
 size_t workspace_bytes_for(const sfm_params &p, const Plan &pl)
 {
@@ -258,7 +250,7 @@ void fill_common(KParams &kp, const sfm_params &p, const Plan &pl)
     kp.split_rows = pl.split_rows;
     kp.path = pl.path;
     kp.fingerprint = (int32_t)fingerprint(p, pl);
-    kp.head_groups = head_groups(p, pl);
+    kp.head_groups = head_groups(p);
     kp.wcap = pl.T * pl.max_splits_per_token;
     kp.max_splits = (int32_t)(pl.max_splits_per_token < INT32_MAX ? pl.max_splits_per_token : INT32_MAX);
 }
@@ -284,6 +276,8 @@ int validate_tensors(const sfm_params &p, const sfm_tensors *t)
     if (!aligned16(t->q) || !aligned16(t->ori_kv)) return SFM_ERR_LAYOUT;
     const int64_t rb = row_bytes(p);
     if (t->ori_row_stride < rb || t->ori_row_stride % 16 || t->ori_rows <= 0) return SFM_ERR_LAYOUT;
+    // the kernel names a KV row with 31 bits (the top bit tells the pools apart)
+    if (t->ori_rows > kMaxPoolRows || (p.has_cmp_kv && t->cmp_rows > kMaxPoolRows)) return SFM_ERR_UNSUPPORTED;
     if (p.has_cmp_kv) {
         if (!t->cmp_kv) return SFM_ERR_INVALID_ARG;
         if (!aligned16(t->cmp_kv)) return SFM_ERR_LAYOUT;
@@ -305,6 +299,70 @@ int validate_tensors(const sfm_params &p, const sfm_tensors *t)
 }
 
 cudaEvent_t g_prof_begin = nullptr, g_prof_end = nullptr;
+
+// sfm_forward() with an optional attended-row dump (sfm_debug_attended):
+// validation, the kernel parameter block, the attention kernel and, when a
+// row can have more than one split, the combine kernel.
+int enqueue_forward(const sfm_params *params, const sfm_tensors *in, const int32_t *metadata, size_t metadata_n,
+                    float softmax_scale, void *out, float *lse, void *workspace, size_t workspace_bytes,
+                    int32_t *status, sfm_stream_t stream, int32_t *dbg_rows, int64_t dbg_cap, int32_t *dbg_counts)
+{
+    int rc = validate_params(params);
+    if (rc) return rc;
+    const sfm_params &p = *params;
+    rc = validate_tensors(p, in);
+    if (rc) return rc;
+    if (!out || !metadata || !isfinite(softmax_scale)) return SFM_ERR_INVALID_ARG;
+    if ((uintptr_t)metadata & 15u) return SFM_ERR_LAYOUT;
+    if (!aligned16(out)) return SFM_ERR_LAYOUT;
+    if (p.return_lse ? !lse : lse != nullptr) return SFM_ERR_INVALID_ARG;
+    Plan pl;
+    rc = make_plan(p, &pl);
+    if (rc) return rc;
+    if (metadata_n < (size_t)meta_words(pl.G, (int)pl.T, pl.T * pl.max_splits_per_token)) return SFM_ERR_WORKSPACE;
+    const size_t need = workspace_bytes_for(p, pl);
+    if (workspace_bytes < need || (need && !workspace) || ((uintptr_t)workspace & 255u)) return SFM_ERR_WORKSPACE;
+
+    KParams kp;
+    fill_common(kp, p, pl);
+    fill_lengths(kp, *in);
+    kp.scale = softmax_scale;
+    kp.scale_log2 = softmax_scale * 1.4426950408889634f;
+    kp.q = in->q;
+    kp.ori_kv = static_cast<const uint8_t *>(in->ori_kv);
+    kp.cmp_kv = static_cast<const uint8_t *>(in->cmp_kv);
+    kp.ori_row_stride = in->ori_row_stride;
+    kp.cmp_row_stride = in->cmp_row_stride;
+    kp.ori_rows = in->ori_rows;
+    kp.cmp_rows = in->cmp_rows;
+    kp.ori_idx = in->ori_sparse_indices;
+    kp.cmp_idx = in->cmp_sparse_indices;
+    kp.ori_bt = in->ori_block_table;
+    kp.cmp_bt = in->cmp_block_table;
+    kp.sinks = in->sinks;
+    kp.meta = metadata;
+    kp.out = out;
+    kp.lse = lse;
+    kp.status = status;
+    kp.dbg_rows = dbg_rows;
+    kp.dbg_cap = dbg_cap;
+    kp.dbg_counts = dbg_counts;
+    if (need) {
+        const int64_t cap = pl.T * pl.max_splits_per_token;
+        kp.ws_capacity_splits = cap;
+        kp.ws_o = static_cast<uint16_t *>(workspace);
+        kp.ws_lse = reinterpret_cast<float *>(static_cast<char *>(workspace) + ws_lse_offset(p, cap));
+    }
+    cudaStream_t st = (cudaStream_t)stream;
+    if (g_prof_begin && cudaEventRecord(g_prof_begin, st) != cudaSuccess) return SFM_ERR_CUDA;
+    if (launch_attn_tc(kp, st) != cudaSuccess) return SFM_ERR_CUDA;
+    if (g_prof_end && cudaEventRecord(g_prof_end, st) != cudaSuccess) return SFM_ERR_CUDA;
+    // at most one split per row: the attention kernel finishes every row
+    // itself (rows without a split included), so there is nothing to merge
+    if (pl.max_splits_per_token > 1 && launch_combine(kp, st) != cudaSuccess) return SFM_ERR_CUDA;
+    return SFM_OK;
+}
+
 
 }  // namespace
 }  // namespace sfm
@@ -385,90 +443,18 @@ int sfm_forward(const sfm_params *params, const sfm_tensors *in, const int32_t *
                 float softmax_scale, void *out, float *lse, void *workspace, size_t workspace_bytes,
                 int32_t *status, sfm_stream_t stream)
 {
-    int rc = validate_params(params);
-    if (rc) return rc;
-    const sfm_params &p = *params;
-    rc = validate_tensors(p, in);
-    if (rc) return rc;
-    if (!out || !metadata || !isfinite(softmax_scale)) return SFM_ERR_INVALID_ARG;
-    if ((uintptr_t)metadata & 15u) return SFM_ERR_LAYOUT;
-    if (!aligned16(out)) return SFM_ERR_LAYOUT;
-    if (p.return_lse ? !lse : lse != nullptr) return SFM_ERR_INVALID_ARG;
-    Plan pl;
-    rc = make_plan(p, &pl);
-    if (rc) return rc;
-    if (metadata_n < (size_t)meta_words(pl.G, (int)pl.T, pl.T * pl.max_splits_per_token)) return SFM_ERR_WORKSPACE;
-    const size_t need = workspace_bytes_for(p, pl);
-    if (workspace_bytes < need || (need && !workspace) || ((uintptr_t)workspace & 255u)) return SFM_ERR_WORKSPACE;
-
-    KParams kp;
-    fill_common(kp, p, pl);
-    fill_lengths(kp, *in);
-    kp.scale = softmax_scale;
-    kp.scale_log2 = softmax_scale * 1.4426950408889634f;
-    kp.q = in->q;
-    kp.ori_kv = static_cast<const uint8_t *>(in->ori_kv);
-    kp.cmp_kv = static_cast<const uint8_t *>(in->cmp_kv);
-    kp.ori_row_stride = in->ori_row_stride;
-    kp.cmp_row_stride = in->cmp_row_stride;
-    kp.ori_rows = in->ori_rows;
-    kp.cmp_rows = in->cmp_rows;
-    kp.ori_idx = in->ori_sparse_indices;
-    kp.cmp_idx = in->cmp_sparse_indices;
-    kp.ori_bt = in->ori_block_table;
-    kp.cmp_bt = in->cmp_block_table;
-    kp.sinks = in->sinks;
-    kp.meta = metadata;
-    kp.out = out;
-    kp.lse = lse;
-    kp.status = status;
-    if (need) {
-        const int64_t cap = pl.T * pl.max_splits_per_token;
-        kp.ws_capacity_splits = cap;
-        kp.ws_o = static_cast<uint16_t *>(workspace);
-        kp.ws_lse = reinterpret_cast<float *>(static_cast<char *>(workspace) + ws_lse_offset(p, cap));
-    }
-    cudaStream_t st = (cudaStream_t)stream;
-    if (g_prof_begin && cudaEventRecord(g_prof_begin, st) != cudaSuccess) return SFM_ERR_CUDA;
-    const cudaError_t le = pl.path == PATH_TC ? launch_attn_tc(kp, st) : launch_attn_simt(kp, st);
-    if (le != cudaSuccess) return SFM_ERR_CUDA;
-    if (g_prof_end && cudaEventRecord(g_prof_end, st) != cudaSuccess) return SFM_ERR_CUDA;
-    // at most one split per row: the tensor-core kernel finishes every row
-    // itself (rows without a split included), so there is nothing to merge
-    const bool merge = pl.path != PATH_TC || pl.max_splits_per_token > 1;
-    if (merge && launch_combine(kp, st) != cudaSuccess) return SFM_ERR_CUDA;
-    return SFM_OK;
+    return enqueue_forward(params, in, metadata, metadata_n, softmax_scale, out, lse, workspace, workspace_bytes,
+                           status, stream, nullptr, 0, nullptr);
 }
 
-int sfm_debug_attended(const sfm_params *params, const sfm_tensors *in, int32_t *rows, int64_t cap,
-                       int32_t *counts, int32_t *status, sfm_stream_t stream)
+int sfm_debug_attended(const sfm_params *params, const sfm_tensors *in, const int32_t *metadata,
+                       size_t metadata_n, float softmax_scale, void *out, float *lse, void *workspace,
+                       size_t workspace_bytes, int32_t *rows, int64_t cap, int32_t *counts, int32_t *status,
+                       sfm_stream_t stream)
 {
-    int rc = validate_params(params);
-    if (rc) return rc;
-    rc = validate_tensors(*params, in);
-    if (rc) return rc;
     if (!rows || !counts || cap <= 0) return SFM_ERR_INVALID_ARG;
-    Plan pl;
-    rc = make_plan(*params, &pl);
-    if (rc) return rc;
-    KParams kp;
-    fill_common(kp, *params, pl);
-    fill_lengths(kp, *in);
-    kp.ori_kv = static_cast<const uint8_t *>(in->ori_kv);
-    kp.cmp_kv = static_cast<const uint8_t *>(in->cmp_kv);
-    kp.ori_row_stride = in->ori_row_stride;
-    kp.cmp_row_stride = in->cmp_row_stride;
-    kp.ori_rows = in->ori_rows;
-    kp.cmp_rows = in->cmp_rows;
-    kp.ori_idx = in->ori_sparse_indices;
-    kp.cmp_idx = in->cmp_sparse_indices;
-    kp.ori_bt = in->ori_block_table;
-    kp.cmp_bt = in->cmp_block_table;
-    kp.status = status;
-    kp.dbg_rows = rows;
-    kp.dbg_cap = cap;
-    kp.dbg_counts = counts;
-    return launch_debug(kp, (cudaStream_t)stream) == cudaSuccess ? SFM_OK : SFM_ERR_CUDA;
+    return enqueue_forward(params, in, metadata, metadata_n, softmax_scale, out, lse, workspace, workspace_bytes,
+                           status, stream, rows, cap, counts);
 }
 
 }  // extern "C"

@@ -1,9 +1,9 @@
 // sfm_internal.cuh -- shared device/host definitions of the sfm library.
 //
-// Everything the planner, the attention kernels, the combine kernel and the
-// debug dump agree on lives here: the kernel parameter block, the metadata
-// layout, the per-query-row lengths and window, and the resolution of an
-// attended position to a KV row address.  The attended set follows the
+// Everything the planner, the attention kernel and the combine kernel agree
+// on lives here: the kernel parameter block, the metadata layout and the
+// per-query-row lengths, window and attended-position counts.  The attended
+// set follows the
 // "sparse_flash_mla" doc (zh), 参数说明 (ori_mask_mode, ori_win_left/right,
 // cmp_mask_mode, cmp_sparse_indices, cmp_residual_kv) and the right-down
 // alignment p = kv_len - q_len + i of its CP切分示例.
@@ -145,7 +145,8 @@ __host__ __device__ inline int64_t meta_words(int G, int T, int64_t wcap)
     return n < 1024 ? 1024 : n;
 }
 
-enum PathId : int32_t { PATH_SIMT = 1, PATH_TC = 2 };
+// the attention path a plan was made for (recorded in the plan header)
+enum PathId : int32_t { PATH_TC = 2 };
 
 // ----------------------------------------------------------------------------
 // kernel parameter block (passed by value)
@@ -168,7 +169,7 @@ struct KParams {
     float scale_log2;                       // softmax_scale * log2(e)
     // plan
     int32_t G, split_rows, fingerprint, path;
-    int32_t head_groups;                    // groups of 64 heads (tensor-core path; 1 otherwise): a token
+    int32_t head_groups;                    // groups of 64 heads: a token
                                             // with n splits owns head_groups * n work units, group-major
     int64_t ws_capacity_splits;
     int32_t max_splits;                     // splits a row can have: row t's partials use workspace
@@ -187,9 +188,9 @@ struct KParams {
     uint16_t *ws_o;   // [slot][512 / 8][q_n][8] normalised partial O, bf16, chunk-major
     float *ws_lse;    // [slot][q_n] partial LSE
     int32_t *status;
-    int32_t *dbg_rows;
+    int32_t *dbg_rows;   // attended-row dump (sfm_debug_attended): [T][dbg_cap] resolver entries, or NULL
     int64_t dbg_cap;
-    int32_t *dbg_counts;
+    int32_t *dbg_counts; // [T] attended positions per row (clamped to dbg_cap)
 };
 
 __device__ __forceinline__ void set_status(const KParams &kp, int bits)
@@ -312,73 +313,6 @@ __device__ inline Tok token_info(const KParams &kp, int t)
     return k;
 }
 
-// ----------------------------------------------------------------------------
-// attended position -> KV row
-// ----------------------------------------------------------------------------
-__device__ __forceinline__ int64_t phys_row(const KParams &kp, int src, int b, int e)
-{
-    if (kp.layout_kv == SFM_LAYOUT_BSND) return (int64_t)b * (src ? kp.cmp_s : kp.ori_s) + e;
-    if (kp.layout_kv == SFM_LAYOUT_TND) return (int64_t)__ldg((src ? kp.cu_cmp : kp.cu_ori) + b) + e;
-    const int bs = src ? kp.cmp_bs : kp.ori_bs;
-    const int32_t *bt = src ? kp.cmp_bt : kp.ori_bt;
-    const int bts = src ? kp.cmp_bt_stride : kp.ori_bt_stride;
-    const int bi = (int)fdiv((uint32_t)e, src ? kp.cmp_bs_div : kp.ori_bs_div);    // e >= 0
-    if (bi >= bts) return -1;     // beyond the block table row
-    const int blk = __ldg(bt + (int64_t)b * bts + bi);
-    if (blk < 0) return -1;
-    return (int64_t)blk * bs + (e - bi * bs);
-}
-
-// Resolve attended position `pos` of query row t.  Returns the row address or
-// nullptr for a skipped entry; *logical receives the ori position or cmp slot
-// (-1 when skipped) and *src 0 (ori) / 1 (cmp).
-__device__ inline const uint8_t *resolve_row(const KParams &kp, const Tok &k, int t, int pos, int *logical,
-                                             int *src)
-{
-    int s, e;
-    bool ok;
-    if (pos < k.n_ori) {
-        s = 0;
-        if (kp.ori_topk > 0) {
-            // entry pos >> sbs_log2 selects a block of 2^sbs_log2 tokens
-            const int idx = __ldg(kp.ori_idx + (int64_t)t * kp.ori_topk + (pos >> kp.sbs_log2));
-            const int64_t tok = ((int64_t)idx << kp.sbs_log2) + (pos & ((1 << kp.sbs_log2) - 1));
-            if (idx >= 0 && ((int64_t)idx << kp.sbs_log2) >= k.kv_len) set_status(kp, SFM_STATUS_BAD_INDEX);
-            ok = idx >= 0 && tok < k.kv_len && tok >= k.lo && tok <= k.hi;
-            e = ok ? (int)tok : -1;
-        } else {
-            e = k.lo + pos;
-            ok = true;
-        }
-    } else {
-        s = 1;
-        const int j = pos - k.n_ori;
-        if (kp.cmp_topk > 0) {
-            e = __ldg(kp.cmp_idx + (int64_t)t * kp.cmp_topk + j);
-            if (e >= k.cmp_len) set_status(kp, SFM_STATUS_BAD_INDEX);
-            ok = e >= 0 && e < k.cmp_len &&
-                 (kp.cmp_mask_mode != 3 || (int64_t)(e + 1) * kp.cmp_ratio <= (int64_t)k.p_cmp + 1);
-        } else {
-            e = j;
-            ok = true;
-        }
-    }
-    *src = s;
-    if (!ok) {
-        *logical = -1;
-        return nullptr;
-    }
-    const int64_t row = phys_row(kp, s, k.b, e);
-    const int64_t nrows = s ? kp.cmp_rows : kp.ori_rows;
-    if (row < 0 || row >= nrows) {
-        set_status(kp, SFM_STATUS_BAD_BLOCK);
-        *logical = -1;
-        return nullptr;
-    }
-    *logical = e;
-    return (s ? kp.cmp_kv : kp.ori_kv) + row * (s ? kp.cmp_row_stride : kp.ori_row_stride);
-}
-
 // metadata sanity check shared by the kernels that consume a plan
 __device__ __forceinline__ bool meta_ok(const KParams &kp)
 {
@@ -431,9 +365,7 @@ inline cudaError_t launch_dependent(void (*kernel)(Args...), dim3 grid, dim3 blo
 // host-side launchers (one per translation unit)
 // ----------------------------------------------------------------------------
 cudaError_t launch_plan(const KParams &kp, cudaStream_t st);
-cudaError_t launch_attn_simt(const KParams &kp, cudaStream_t st);
 cudaError_t launch_attn_tc(const KParams &kp, cudaStream_t st);
 cudaError_t launch_combine(const KParams &kp, cudaStream_t st);
-cudaError_t launch_debug(const KParams &kp, cudaStream_t st);
 
 }  // namespace sfm

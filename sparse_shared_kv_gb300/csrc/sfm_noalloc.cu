@@ -13,34 +13,25 @@
 // on the GPU (different streams without ordering between them) race on it.
 // Nothing in it needs to start at zero: each split writes its partial result
 // before the combine kernel of the same call reads it.
-#include <mutex>
-
 #include "sfm_internal.cuh"
 
 namespace {
 
 constexpr size_t kStaticWorkspaceBytes = SFM_NOALLOC_WORKSPACE_BYTES;
-constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_static_workspace[kStaticWorkspaceBytes];
 
-// Device address of g_static_workspace, resolved once per device.  In host
-// code the symbol itself is only a host-side stand-in, never a device pointer.
-void *g_workspace_addr[kMaxDevices] = {};
-std::mutex g_workspace_mu;
-
+// Device address of g_static_workspace on the current device.  In host code
+// the symbol itself is only a host-side stand-in, never a device pointer.  The
+// address is looked up on every call rather than cached: the lookup allocates
+// nothing, and after a device reset (or any re-creation of the primary
+// context) the module is loaded again at a new address, which a cached
+// pointer would not follow.  The first call on a device loads the module.
 int static_workspace(void **out)
 {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return SFM_ERR_CUDA;
-    if (dev < 0 || dev >= kMaxDevices) return SFM_ERR_UNSUPPORTED;
-    std::lock_guard<std::mutex> lock(g_workspace_mu);
-    if (!g_workspace_addr[dev]) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_static_workspace) != cudaSuccess || !p) return SFM_ERR_CUDA;
-        g_workspace_addr[dev] = p;
-    }
-    *out = g_workspace_addr[dev];
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_static_workspace) != cudaSuccess || !p) return SFM_ERR_CUDA;
+    *out = p;
     return SFM_OK;
 }
 

@@ -52,36 +52,51 @@ def run(prob):
     return Runner(prob).run()
 
 
-def debug_sets(prob, cap=None):
-    """Resolved attended rows per token as [(src, pos), ...] in kernel order."""
-    params = params_of(prob)
-    tens = tensors_of(prob)
-    if cap is None:
-        cap = 1
-        for name in ("ori_sparse_indices", "cmp_sparse_indices"):
-            x = prob.t[name]
-            if x is not None:                       # ori entries select sparse_block_size tokens each
-                cap += x.shape[-1] * (prob.sparse_block_size if name == "ori_sparse_indices" else 1)
-        if prob.ori_topk == 0:
-            w = prob.max_seqlen_ori_kv
-            if prob.ori_mask_mode == 4 and prob.ori_win_left >= 0 and prob.ori_win_right >= 0:
-                w = min(w, prob.ori_win_left + prob.ori_win_right + 1)
-            cap += w
-        if prob.has_cmp_kv and prob.cmp_topk == 0:
-            cap += prob.max_seqlen_cmp_kv
+def _dump_cap(prob):
+    """Upper bound of attended positions per query row."""
+    cap = 1
+    for name in ("ori_sparse_indices", "cmp_sparse_indices"):
+        x = prob.t[name]
+        if x is not None:                       # ori entries select sparse_block_size tokens each
+            cap += x.shape[-1] * (prob.sparse_block_size if name == "ori_sparse_indices" else 1)
+    if prob.ori_topk == 0:
+        w = prob.max_seqlen_ori_kv
+        if prob.ori_mask_mode == 4 and prob.ori_win_left >= 0 and prob.ori_win_right >= 0:
+            w = min(w, prob.ori_win_left + prob.ori_win_right + 1)
+        cap += w
+    if prob.has_cmp_kv and prob.cmp_topk == 0:
+        cap += prob.max_seqlen_cmp_kv
+    return cap
+
+
+UNWRITTEN = -2
+
+
+def debug_rows(prob, cap=None):
+    """The KV rows the attention kernel's resolver handed to its copy warps,
+    per query row, through sfm_debug_attended (the real forward with its dump
+    on).  Returns (entries, out, lse, status): entries[t] is the int32 array
+    of positions 0..counts[t]-1 (-1 skipped, r an ori pool row, r | 1 << 31 a
+    cmp pool row; UNWRITTEN where the kernel wrote nothing)."""
+    r = Runner(prob)
+    cap = cap or _dump_cap(prob)
     dev = prob.t["q"].device
-    rows = torch.full((prob.num_tokens, cap), -2, dtype=torch.int32, device=dev)
+    rows = torch.full((prob.num_tokens, cap), UNWRITTEN, dtype=torch.int32, device=dev)
     counts = torch.zeros(prob.num_tokens, dtype=torch.int32, device=dev)
-    status = torch.zeros(1, dtype=torch.int32, device=dev)
-    sfm.sfm_debug_attended(params, tens, rows, cap, counts, status)
+    r.status.zero_()
+    r.plan()
+    sfm.sfm_debug_attended(r.params, r.tensors, r.meta, prob.softmax_scale, r.out, r.lse, r.ws, rows, cap, counts,
+                           r.status)
     torch.cuda.synchronize()
     rows = rows.cpu().numpy()
     counts = counts.cpu().numpy()
-    out = []
-    for t in range(prob.num_tokens):
-        r = rows[t, :counts[t]]
-        r = r[r >= 0]
-        src = (r >> 30) & 1
-        pos = r & 0x3FFFFFFF
-        out.append((src.astype(np.int32), pos.astype(np.int32)))
-    return out, int(status.item())
+    entries = [rows[t, :counts[t]].copy() for t in range(prob.num_tokens)]
+    return entries, r.out, r.lse, int(r.status.item())
+
+
+def split_entries(e):
+    """(src, pool row) of the attended entries of one dump row, skipped ones dropped."""
+    e = e[e != -1]
+    src = (e < 0).astype(np.int32)                       # bit 31: the compressed pool
+    row = (e.astype(np.int64) & 0x7FFFFFFF).astype(np.int64)
+    return src, row

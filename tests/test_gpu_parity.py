@@ -5,7 +5,9 @@ Tolerances (bf16 / fp16 inputs, fp32 accumulation, bf16 / fp16 output):
 1e-3; rows with an empty attended set must give exactly 0 and -inf.  FP8
 packed rows add to the LSE bound the change that the one fp16 rounding of
 K~ = e4m3 x scale causes by itself (see _fp8_lse_slack).  Attended
-row sets are compared exactly through the library's debug dump.
+row sets are compared exactly: the attention kernel's resolver records every
+KV row it hands to its copy warps (sfm_debug_attended) and the sequence must
+equal the oracle's attended set mapped to pool rows.
 """
 import math
 
@@ -94,17 +96,43 @@ def assert_parity(prob, out, lse, tokens=None, host=None):
     return err.max()
 
 
-def assert_sets(prob, tokens=None, host=None):
+def _pool_rows(host, t, src, pos):
+    """Pool rows of the oracle's attended (src, pos) of token t, through the
+    layout (and block table) by the test's own mapping."""
+    b = _brute.lengths(host, t)[0]
+    rows = np.zeros(len(pos), dtype=np.int64)
+    for s_, which in ((0, "ori_kv"), (1, "cmp_kv")):
+        m = src == s_
+        if m.any():
+            rows[m] = _brute._physical(host, which, b, int(pos[m].max()) + 1)[pos[m]]
+    return rows
+
+
+def assert_sets(prob, tokens=None, host=None, out=None, lse=None):
+    """Exact attended sets of the attention kernel itself: the rows its
+    resolver handed to the copy warps (sfm_debug_attended), in position
+    order, against the oracle's attended set mapped to pool rows; every
+    attended position must have been written.  With out / lse given, the
+    dump call's outputs must equal them bit for bit (the dump does not change
+    the computation)."""
     host = host or prob.to("cpu")
-    sets, status = _sfm.debug_sets(prob)
+    entries, o_dbg, l_dbg, status = _sfm.debug_rows(prob)
     assert status & ~sfm.STATUS_BAD_INDEX == 0, hex(status)
+    if out is not None:
+        assert torch.equal(o_dbg, out), f"{prob.name}: output of the dump call differs"
+    if lse is not None:
+        assert torch.equal(l_dbg, lse), f"{prob.name}: LSE of the dump call differs"
     if tokens is None:
         tokens = range(prob.num_tokens)
     b = oracle._Bound(host)
     for t in tokens:
         src, pos = oracle.attended(host, t, b)
-        gs, gp = sets[t]
-        assert np.array_equal(gs, src) and np.array_equal(gp, pos), f"{prob.name}: token {t} attended set differs"
+        e = entries[t]
+        assert (e != _sfm.UNWRITTEN).all(), f"{prob.name}: token {t}: attended positions the resolver never wrote"
+        gs, gr = _sfm.split_entries(e)
+        want = _pool_rows(host, t, src, pos)
+        assert np.array_equal(gs, src) and np.array_equal(gr, want), \
+            f"{prob.name}: token {t}: resolved rows differ from the oracle's attended set"
 
 
 # ---------------------------------------------------------------------------
@@ -122,7 +150,7 @@ def test_tiny_parity_and_sets(name, kw):
     expected = sfm.STATUS_BAD_INDEX if name == "csa_tnd_any_idx" else 0
     assert status == expected, hex(status)
     assert_parity(prob, out, lse)
-    assert_sets(prob)
+    assert_sets(prob, out=out, lse=lse)
 
 
 @pytest.mark.parametrize("q_n", [1, 2, 8, 16, 32, 48, 64, 128])
@@ -153,7 +181,21 @@ def test_reduced_workloads(key):
     assert status == 0, hex(status)
     host = prob.to("cpu")
     assert_parity(prob, out, lse, host=host)
-    assert_sets(prob, host=host)
+    assert_sets(prob, host=host, out=out, lse=lse)
+
+
+@pytest.mark.parametrize("batch", [4, 32], ids=["reduced", "full_size"])
+def test_csa_topk_1024(batch):
+    """CSA with 1024 compressed indices per query, the second top-k size the
+    pages allow for cmp_sparse_indices (512 or 1024): every row of a reduced
+    batch, sampled rows of the full-size decode batch, sets exactly."""
+    prob = S.csa_decode(device="cuda", batch=batch, cmp_topk=1024, seed=9)
+    out, lse, status = _sfm.run(prob)
+    assert status == 0, hex(status)
+    host = prob.to("cpu")
+    tokens = None if batch <= 4 else _sample(prob, 12)
+    assert_parity(prob, out, lse, tokens=tokens, host=host)
+    assert_sets(prob, tokens=tokens, host=host, out=out, lse=lse)
 
 
 def test_fp16_and_lse_off():
@@ -187,7 +229,7 @@ def test_full_size_sampled(key):
     tokens = _sample(prob, 24 if key != "csa_prefill" else 64, extra)
     host = prob.to("cpu")
     assert_parity(prob, out, lse, tokens=tokens, host=host)
-    assert_sets(prob, tokens=tokens, host=host)
+    assert_sets(prob, tokens=tokens, host=host, out=out, lse=lse)
     # properties that hold at any size: finite outputs, LSE finite where rows attend something
     assert torch.isfinite(out.float()).all()
 
@@ -296,6 +338,32 @@ def test_metadata_mismatch_zeroes_outputs_without_combine():
     assert torch.count_nonzero(r.out.float()) == 0 and torch.isneginf(r.lse).all()
 
 
+@pytest.mark.parametrize("return_lse", [False, True], ids=["lse_off", "lse_on"])
+@pytest.mark.parametrize("fmt", ["int8_packed", "fp8_packed"])
+def test_packed_128_heads_row_without_positions(fmt, return_lse):
+    """128-head packed decode plans have at most one split per row, so no
+    combine kernel runs: the attention kernel itself must write the row with
+    no attended position (kv_len 0) as O = 0 (and LSE = -inf when returned)
+    and leave the status clean."""
+    prob = S.build("packed_empty", seed=88, device="cuda", q_n=128, q_lens=[1, 1, 1], kv_lens=[900, 0, 1500],
+                   layout_q="BSND", layout_kv="PAGED", mode="ori_sparse", ori_topk=256, ori_mask_mode=3,
+                   cmp_mask_mode=0, kv_format=fmt, rope_head_dim=64, ori_block_size=64, sinks=True,
+                   return_lse=return_lse)
+    r = _sfm.Runner(prob)
+    assert sfm.sfm_workspace_size(r.params) == 0          # one split per row: no combine launch
+    r.out.fill_(float("nan"))
+    if r.lse is not None:
+        r.lse.fill_(float("nan"))
+    out, lse, status = r.run()
+    assert status == 0, hex(status)
+    assert (lse is None) == (not return_lse)
+    assert torch.count_nonzero(out[1].float()) == 0
+    if lse is not None:
+        assert torch.isneginf(lse[1]).all()
+    assert_parity(prob, out, lse)
+    assert_sets(prob, out=out, lse=lse)
+
+
 def test_public_two_call_api():
     prob = S.csa_decode(device="cuda", batch=3)
     T = prob.t
@@ -373,58 +441,58 @@ def test_two_call_api_in_cuda_graphs_on_two_streams():
 
 
 # ---------------------------------------------------------------------------
-# both attention kernels on the shapes the tensor-core kernel covers
+# the attention kernel's code paths: head counts, split counts, dtypes,
+# block-wise selection, packed formats
 # ---------------------------------------------------------------------------
 def _plain_cases():
     return [c for c in _tiny_cases() if "packed" not in c[0]]
 
 
-@pytest.mark.parametrize("hint", [1, 2], ids=["cuda_core", "tensor_core"])
 @pytest.mark.parametrize("name,kw", _plain_cases(), ids=[c[0] for c in _plain_cases()])
-def test_kernel_paths_tiny(name, kw, hint):
+def test_kernel_paths_tiny(name, kw):
     prob = S.build(name, seed=17, q_n=4, device="cuda", **kw)
-    out, lse, status = _sfm.Runner(prob, params=_sfm.params_of(prob, kernel_hint=hint)).run()
+    out, lse, status = _sfm.run(prob)
     assert status == 0, hex(status)
     assert_parity(prob, out, lse)
+    assert_sets(prob, out=out, lse=lse)
 
 
-@pytest.mark.parametrize("hint", [1, 2], ids=["cuda_core", "tensor_core"])
 @pytest.mark.parametrize("q_n", [1, 8, 16, 32, 40, 64, 65, 96, 128])
-def test_kernel_paths_heads(q_n, hint):
+def test_kernel_paths_heads(q_n):
     prob = S.build(f"heads{q_n}", seed=100 + q_n, device="cuda", q_n=q_n, q_lens=[1, 1, 1, 1],
                    kv_lens=[700, 1500, 300, 20000], layout_q="BSND", layout_kv="PAGED", mode="csa", cmp_ratio=4,
                    cmp_topk=384, sinks=True)
-    out, lse, status = _sfm.Runner(prob, params=_sfm.params_of(prob, kernel_hint=hint)).run()
+    out, lse, status = _sfm.run(prob)
     assert status == 0, hex(status)
     assert_parity(prob, out, lse)
+    assert_sets(prob, out=out, lse=lse)
 
 
-@pytest.mark.parametrize("hint", [1, 2], ids=["cuda_core", "tensor_core"])
-def test_many_splits_and_single_split_rows(hint):
+def test_many_splits_and_single_split_rows():
     # a causal decode batch mixing a row of 6000 positions (dozens of splits:
     # the combine's looped merge past its unrolled case), a row of one split
     # (written directly by the attention kernel) and rows in between
     prob = S.build("many_splits", seed=61, device="cuda", q_n=64, q_lens=[1, 1, 1, 1],
                    kv_lens=[6000, 100, 1300, 2600], layout_q="BSND", layout_kv="PAGED", mode="swa",
                    ori_mask_mode=3, win_left=-1, win_right=-1, sinks=True)
-    out, lse, status = _sfm.Runner(prob, params=_sfm.params_of(prob, kernel_hint=hint)).run()
+    out, lse, status = _sfm.run(prob)
     assert status == 0, hex(status)
     assert_parity(prob, out, lse)
+    assert_sets(prob, out=out, lse=lse)
 
 
-@pytest.mark.parametrize("hint", [1, 2], ids=["cuda_core", "tensor_core"])
-def test_kernel_paths_prefill_fp16(hint):
+def test_kernel_paths_prefill_fp16():
     prob = S.build("prefill_fp16", seed=23, device="cuda", q_n=64, q_lens=[70, 130], kv_lens=[200, 900],
                    layout_q="TND", layout_kv="PAGED", mode="hca", cmp_ratio=4, dtype="fp16", sinks=True,
                    ori_block_size=64, cmp_block_size=32)
-    out, lse, status = _sfm.Runner(prob, params=_sfm.params_of(prob, kernel_hint=hint)).run()
+    out, lse, status = _sfm.run(prob)
     assert status == 0, hex(status)
     assert_parity(prob, out, lse)
+    assert_sets(prob, out=out, lse=lse)
 
 
 @pytest.mark.parametrize("sbs", [2, 16, 64])
-@pytest.mark.parametrize("hint", [1, 2], ids=["cuda_core", "tensor_core"])
-def test_blockwise_selection(sbs, hint):
+def test_blockwise_selection(sbs):
     # block-wise top-k over a paged packed pool (each index selects sbs
     # consecutive tokens, masked per token by right-down causality); indices
     # include masked (-1), partly visible and out-of-range blocks
@@ -433,17 +501,17 @@ def test_blockwise_selection(sbs, hint):
                    ori_topk=2048 // sbs, ori_mask_mode=3, cmp_mask_mode=0, kv_format="int8_packed",
                    rope_head_dim=64, ori_block_size=64, sparse_block_size=sbs, index_mode="any",
                    softmax_scale=1.0 / 24.0)
-    out, lse, status = _sfm.Runner(prob, params=_sfm.params_of(prob, kernel_hint=hint)).run()
+    out, lse, status = _sfm.run(prob)
     assert status in (0, 1), hex(status)
     assert_parity(prob, out, lse)
-    assert_sets(prob)
+    assert_sets(prob, out=out, lse=lse)
 
 
 @pytest.mark.parametrize("fmt", ["int8_packed", "fp8_packed"])
 def test_rope0_rows_equal_zero_padded_rows(fmt):
     """Compact 528-byte rows (rope_head_dim 0, q of 512 dims) against the same
     NoPE bytes and scales in 656-byte rows with a zero rope part and q's rope
-    part zero: bit for bit the same output and LSE on the tensor-core kernel
+    part zero: bit for bit the same output and LSE
     (the kv_quant guide's rope-0 test compares the two with torch.equal)."""
     kw = dict(seed=77, device="cuda", q_n=64, q_lens=[1, 1], kv_lens=[1200, 700], layout_q="BSND",
               layout_kv="PAGED", mode="ori_sparse", ori_topk=256, ori_mask_mode=3, cmp_mask_mode=0,
@@ -462,8 +530,8 @@ def test_rope0_rows_equal_zero_padded_rows(fmt):
     q[..., :512] = p0.t["q"]
     q[..., 512:] = 0
     p64.softmax_scale = p0.softmax_scale
-    o64, l64, st64 = _sfm.Runner(p64, params=_sfm.params_of(p64, kernel_hint=2)).run()
-    o0, l0, st0 = _sfm.Runner(p0, params=_sfm.params_of(p0, kernel_hint=2)).run()
+    o64, l64, st64 = _sfm.run(p64)
+    o0, l0, st0 = _sfm.run(p0)
     assert st64 == 0 and st0 == 0
     assert torch.equal(o64, o0) and torch.equal(l64, l0)
     assert_parity(p0, o0, l0)
@@ -471,15 +539,15 @@ def test_rope0_rows_equal_zero_padded_rows(fmt):
 
 @pytest.mark.parametrize("rope", [0, 64])
 @pytest.mark.parametrize("fmt", ["int8_packed", "fp8_packed"])
-@pytest.mark.parametrize("hint", [1, 2], ids=["cuda_core", "tensor_core"])
 @pytest.mark.parametrize("q_n", [16, 64, 128])
-def test_kernel_paths_packed(q_n, hint, fmt, rope):
+def test_kernel_paths_packed(q_n, fmt, rope):
     # packed int8 / E4M3 rows (656 bytes) with token-wise top-k over a paged
     # pool; the index lists include masked (-1) and future entries
     prob = S.build(f"packed{q_n}", seed=300 + q_n, device="cuda", q_n=q_n, q_lens=[1, 1, 1], kv_lens=[900, 3000, 200],
                    layout_q="BSND", layout_kv="PAGED", mode="ori_sparse", ori_topk=256, ori_mask_mode=3,
                    cmp_mask_mode=0, kv_format=fmt, rope_head_dim=rope, ori_block_size=64,
                    index_mode="any", softmax_scale=1.0 / 24.0)
-    out, lse, status = _sfm.Runner(prob, params=_sfm.params_of(prob, kernel_hint=hint)).run()
+    out, lse, status = _sfm.run(prob)
     assert status in (0, 1), hex(status)       # out-of-range indices are flagged (BAD_INDEX) and skipped
     assert_parity(prob, out, lse)
+    assert_sets(prob, out=out, lse=lse)

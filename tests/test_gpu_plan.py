@@ -148,13 +148,12 @@ CASES = {
 }
 
 
-@pytest.mark.parametrize("hint", [1, 2], ids=["cuda_core", "tensor_core"])
 @pytest.mark.parametrize("name", list(CASES))
-def test_plan_words(name, hint):
+def test_plan_words(name):
     kw = dict(CASES[name])
     q_n = kw.pop("q_n")
     prob = S.build(name, seed=71, device="cuda", q_n=q_n, **kw)
-    r = _sfm.Runner(prob, params=_sfm.params_of(prob, kernel_hint=hint))
+    r = _sfm.Runner(prob)
     r.plan()
     torch.cuda.synchronize()
     W, G = check_plan(prob, r.meta, q_n)
