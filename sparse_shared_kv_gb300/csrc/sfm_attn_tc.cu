@@ -85,10 +85,15 @@ constexpr int kPrefetchTiles = 4;            // tiles past the stages whose rows
 
 // Shared-memory layout.  Plain rows: Q (8 column blocks of 64 values), P,
 // four 32-row bf16 stages.  Packed rows: Q and K carry 9 column blocks (512
-// dequantized values + 64 rope values), two bf16 stages and two raw stages
-// of 32 packed rows (the copy target the producers convert from).
-template <bool PK>
+// NoPE values + 64 rope values), two fp16 stages, two raw stages of 32
+// packed rows (the copy target the producers convert from) and each fp16
+// stage's per-row scales (4 per row, one per 128-value tile).
+// MODE 0: plain rows; 1: packed rows whose dequantised values are rounded
+// once to fp16 (int8); 2: packed rows computed from their exact unscaled
+// values with the scales applied in fp32 (E4M3).
+template <int MODE>
 struct Lay {
+    static constexpr bool PK = MODE > 0;
     static constexpr int QB = PK ? 9 : 8;                        // 64-column blocks of a Q / K row
     static constexpr int kStages = PK ? 2 : 4;                   // bf16 KV stages == S buffers
     static constexpr uint32_t Q_OFF = 0;                         // QB blocks x 64 rows x 128 B
@@ -97,7 +102,9 @@ struct Lay {
     static constexpr uint32_t KV_COL = kStages * KV_BLOCK;       // stride between 64-column blocks
     static constexpr uint32_t RAW_OFF = KV_OFF + QB * KV_COL;
     static constexpr uint32_t RAW_STAGE = NT * PK_ROW;
-    static constexpr uint32_t MISC_OFF = (RAW_OFF + (PK ? 2 * RAW_STAGE : 0) + 1023u) & ~1023u;
+    static constexpr uint32_t SCL_OFF = RAW_OFF + (PK ? 2 * RAW_STAGE : 0);   // [stage][tile][32 rows] fp32 scales
+    static constexpr uint32_t SCL_BYTES = MODE == 2 ? kStages * 4 * NT * 4 : 0;
+    static constexpr uint32_t MISC_OFF = (SCL_OFF + SCL_BYTES + 1023u) & ~1023u;
     static constexpr uint32_t EPI_OFF = MISC_OFF + MISC_BYTES;   // epilogue staging, 1 KB per softmax warp
     static constexpr uint32_t kSmemBytes = EPI_OFF + 4 * 1024 + 1024;   // + alignment slack
     static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -122,16 +129,17 @@ enum Bar {
     B_TEARDOWN_PV = 60,
     B_TEARDOWN_S2 = 61,
     B_TEARDOWN_S3 = 62,
-    kNumBars = 63
+    B_SV_DONE = 63,    // [2] packed rows: every S product of the tile on that stage has read it
+    kNumBars = 65
 };
 // offsets inside the misc area
-constexpr uint32_t TMEM_SLOT_REL = 512;
-constexpr uint32_t ABORT_REL = 516;
-constexpr uint32_t VALID_REL = 528;      // [4] row-valid words
+constexpr uint32_t TMEM_SLOT_REL = 576;
+constexpr uint32_t ABORT_REL = 580;
+constexpr uint32_t VALID_REL = 592;      // [4] row-valid words
 constexpr uint32_t ALPHA_REL = 1024;     // [4][64] floats
 constexpr uint32_t STATS_REL = 2048;     // [64][2] floats
 constexpr uint32_t RING_REL = 2560;      // [16][32] int32 row entries
-static_assert(kNumBars * 8 <= 512, "barrier area");
+static_assert(kNumBars * 8 <= TMEM_SLOT_REL && VALID_REL + 16 <= 1024, "barrier area");
 static_assert(RING_REL + kRing * NT * 4 <= MISC_BYTES, "misc area");
 
 struct Unit {
@@ -335,21 +343,28 @@ __device__ __noinline__ void finish_rows_without_split(const int32_t *meta, bool
     }
 }
 
-template <bool PK>
+template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(const KParams kp)
 {
-    using L = Lay<PK>;
+    using L = Lay<MODE>;
+    constexpr bool PK = MODE > 0;          // packed rows
+    constexpr bool EX = MODE == 2;         // packed rows with exact scores
     constexpr int QB = L::QB, kStages = L::kStages;
-    // independent accumulation chains of S (TMEM: chain c, stage s at
-    // TM_S + 32 (c * kStages + s)); packed rows have two stages, which leaves
-    // room for four shorter chains
-    constexpr int kChains = PK ? 3 : 2;
-    // S is issued by one warp per chain: the tensor pipe takes products from
+    // Independent accumulation chains of S (TMEM: chain c, buffer b at
+    // TM_S + 32 (c * kSBufs + b)).  Plain rows: two chains (dimensions 0-255
+    // and 256-511), one buffer per stage, issued by warps 8 and 10.  Packed
+    // rows rounded to fp16: three chains of 192 dimensions (warps 8, 10, 11).
+    // Packed rows with exact scores: one chain per 128-value scale tile and
+    // one for the rope part, so that the products are exact products of the
+    // unscaled values and the softmax applies each row's fp32 tile scales;
+    // five chains leave room for one buffer only, issued by warps 8 (tiles 0,
+    // 1), 10 (tiles 2, 3) and 11 (rope).  The tensor pipe takes products from
     // several issuing warps at once, while one warp issues one about every
-    // 100-130 ns whatever its size (warps 8 and 10; packed rows also warp 11)
-    constexpr int kIssuers = kChains;
-    static_assert(kChains * kStages * NT <= 256, "S buffers fit next to O in TMEM");
-    static_assert((QB * 4) % kChains == 0, "reduction steps split evenly over the chains");
+    // 100-130 ns whatever its size.
+    constexpr int kChains = EX ? 5 : PK ? 3 : 2;
+    constexpr int kIssuers = PK ? 3 : 2;
+    constexpr int kSBufs = EX ? 1 : kStages;
+    static_assert(kChains * kSBufs * NT <= 256, "S buffers fit next to O in TMEM");
     constexpr uint32_t Q_OFF = L::Q_OFF, P_OFF = L::P_OFF, KV_COL = L::KV_COL, MISC_OFF = L::MISC_OFF;
     constexpr uint32_t EPI_OFF = L::EPI_OFF, TMEM_SLOT_OFF = MISC_OFF + TMEM_SLOT_REL, ABORT_OFF = MISC_OFF + ABORT_REL;
     constexpr uint32_t VALID_OFF = MISC_OFF + VALID_REL, ALPHA_OFF = MISC_OFF + ALPHA_REL;
@@ -364,6 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(const KParams 
     auto bar = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
     volatile int *abort_flag = reinterpret_cast<volatile int *>(base + ABORT_OFF);
     uint32_t *valid_s = reinterpret_cast<uint32_t *>(base + VALID_OFF);
+    float *scl = reinterpret_cast<float *>(base + L::SCL_OFF);     // packed rows: [stage][tile][row] scales
     float *alpha_s = reinterpret_cast<float *>(base + ALPHA_OFF);
     float *stats_s = reinterpret_cast<float *>(base + STATS_OFF);
 
@@ -402,6 +418,7 @@ __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(const KParams 
         mbar_init(bar(B_TEARDOWN_PV), 1);
         mbar_init(bar(B_TEARDOWN_S2), 1);
         mbar_init(bar(B_TEARDOWN_S3), 1);
+        for (int s = 0; s < 2; ++s) mbar_init(bar(B_SV_DONE + s), kIssuers);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -417,8 +434,10 @@ __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(const KParams 
 
     // While the planner still runs: pull this CTA's share of the index
     // tensors, block tables and Q into L2 (they do not depend on the plan),
-    // so the first dependent loads after the plan hit L2.
-    if (tid == 9 * 32) {
+    // so the first dependent loads after the plan hit L2.  Issued by a lane
+    // of an S-issuing warp, which has nothing to do until the first tile
+    // lands (issuing these from the resolver delayed its first loads).
+    if (tid == 10 * 32 + 1) {
         const int G = gridDim.x, c = blockIdx.x;
         constexpr int64_t kCap = 256 * 1024;
         prefetch_share(kp.cmp_idx, (int64_t)kp.T * kp.cmp_topk * 4, c, G, kCap);
@@ -452,14 +471,19 @@ __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(const KParams 
         // and publishes each tile's 32 entries in ring slot (tile % kRing).
         int g = 0;
         bool stop = false;
+        const bool pf_all = !PK && kp.split_rows < (1 << 30);     // plain rows, decode-shaped plan
         Unit cur = first;
         for (int u = u_beg; u < u_end && !stop; ++u) {
             const Unit nxt = u + 1 < u_end ? unit_info(kp, sp, u + 1) : cur;   // prefetched
             const Unit &s = cur;
-            // publish tiles i0 .. i0 + K - 1 of the unit, then pull the rows
-            // of the worker's tiles kStages .. kStages + kPrefetchTiles - 1
-            // into L2: those tiles wait for a stage to drain before their
-            // copies start, and then hit L2
+            // publish tiles i0 .. i0 + K - 1 of the unit, then pull into L2
+            // the rows of the tiles that wait for a stage to drain before
+            // their copies start, so that those copies hit L2: for plain
+            // rows of decode-shaped plans every tile from kStages on,
+            // otherwise the worker's tiles kStages .. kStages +
+            // kPrefetchTiles - 1 (prefill rows share most of their rows, and
+            // more prefetching only added traffic there); one bulk prefetch
+            // per plain row, line prefetches for packed rows
             auto publish = [&](int i0, int K, const int32_t *ent) {
                 if (kp.dbg_rows) {
                     // attended-row dump: the entries exactly as the copy warps
@@ -488,13 +512,17 @@ __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(const KParams 
                 }
                 for (int j = 0; j < K; ++j) {
                     const int gi = g + i0 + j;
-                    if (i0 + j < s.ntiles && gi >= kStages && gi < kStages + kPrefetchTiles && ent[j] != -1) {
+                    if (i0 + j < s.ntiles && gi >= kStages && (pf_all || gi < kStages + kPrefetchTiles) && ent[j] != -1) {
                         const int64_t r = ent[j] & 0x7fffffff;
                         const uint8_t *row = ent[j] < 0 ? kp.cmp_kv + r * kp.cmp_row_stride : kp.ori_kv + r * kp.ori_row_stride;
                         constexpr uint32_t kRowBytes = PK ? PK_ROW : QB * 128u;
+                        if constexpr (!PK) {
+                            prefetch_l2(row, kRowBytes);         // one bulk prefetch per 1 KB row
+                        } else {
 #pragma unroll
-                        for (uint32_t o = 0; o < kRowBytes; o += 128) prefetch_line_l2(row + o);
-                        prefetch_line_l2(row + kRowBytes - 1);
+                            for (uint32_t o = 0; o < kRowBytes; o += 128) prefetch_line_l2(row + o);
+                            prefetch_line_l2(row + kRowBytes - 1);
+                        }
                     }
                 }
             };
@@ -600,21 +628,28 @@ __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(const KParams 
                 const float sc = *reinterpret_cast<const float *>(row + scale_off + 4 * (lane >> 3));
                 const uint32_t w[4] = {v.x, v.y, v.z, v.w};
                 uint32_t o[8];
+                // MODE 1: value x scale in fp32, rounded once to fp16.
+                // MODE 2: the unscaled values (every int8 and every E4M3
+                // value is an fp16 value, so the conversion is exact); the
+                // scale is applied in fp32 to the products (S) and, after S
+                // has read the stage, to the values in place (for P.V)
+                const float vs = EX ? 1.f : sc;
                 if (fp8) {
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
                         float f[4];
                         e4m3x4_to_f32(w[q], f);
-                        o[2 * q] = pack2(f[0] * sc, f[1] * sc, false);
-                        o[2 * q + 1] = pack2(f[2] * sc, f[3] * sc, false);
+                        o[2 * q] = pack2(f[0] * vs, f[1] * vs, false);
+                        o[2 * q + 1] = pack2(f[2] * vs, f[3] * vs, false);
                     }
                 } else {
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
-                        o[2 * q] = pack2(i8_to_f32(w[q], 0) * sc, i8_to_f32(w[q], 1) * sc, false);
-                        o[2 * q + 1] = pack2(i8_to_f32(w[q], 2) * sc, i8_to_f32(w[q], 3) * sc, false);
+                        o[2 * q] = pack2(i8_to_f32(w[q], 0) * vs, i8_to_f32(w[q], 1) * vs, false);
+                        o[2 * q + 1] = pack2(i8_to_f32(w[q], 2) * vs, i8_to_f32(w[q], 3) * vs, false);
                     }
                 }
+                if (EX && (lane & 7) == 0) scl[(st * 4 + (lane >> 3)) * NT + rr] = sc;
                 const uint32_t dst = sb + kv_at(st, lane >> 2);
                 *reinterpret_cast<uint4 *>(base + (dst - sb) + sw128(rr, (lane & 3) * 2)) = make_uint4(o[0], o[1], o[2], o[3]);
                 *reinterpret_cast<uint4 *>(base + (dst - sb) + sw128(rr, (lane & 3) * 2 + 1)) =
@@ -710,13 +745,16 @@ __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(const KParams 
     } else if (warp == 8 || warp == 10 || (kIssuers > 2 && warp == 11)) {
         // ======================= S issuers =======================
         // S(i) needs tile i staged and its S buffer free.  Its reduction
-        // steps run as independent accumulation chains, one per issuing warp:
-        // plain rows warps 8 and 10 (dimensions 0..255 and 256..511), packed
-        // rows warps 8, 10 and 11 (192 of the 576 dimensions each), into TMEM
-        // column ranges chain c, stage st at TM_S + 32 (c kStages + st); the
-        // softmax adds them.  An even tile and the next tile of the same unit
-        // are computed together as one N=64 product, which halves the number
-        // of S instructions (the tensor pipe's instruction rate, not its math,
+        // steps run as independent accumulation chains: plain rows one per
+        // issuing warp, warps 8 and 10 (dimensions 0..255 and 256..511), into
+        // TMEM column ranges chain c, stage st at TM_S + 32 (c kStages + st);
+        // packed rows five chains (the four 128-value scale tiles and the rope
+        // part) into one buffer, TM_S + 32 c, warp 8 issuing tiles 0 and 1,
+        // warp 10 tiles 2 and 3 (interleaved), warp 11 the rope part.  The
+        // softmax adds the chains (packed rows: with each row's tile scales).
+        // For plain rows an even tile and the next tile of the same unit are
+        // computed together as one N=64 product, which halves the number of
+        // S instructions (the tensor pipe's instruction rate, not its math,
         // bounds these small products).  P.V is issued by warp 6.
         if (lane == 0) {
             const int c = warp == 8 ? 0 : warp == 10 ? 1 : 2;     // this warp's chain
@@ -742,9 +780,11 @@ __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(const KParams 
                     // and stop the conversion of the next tile from overlapping)
                     const int nt = (!PK && (gi & 1) == 0 && i + 1 < s.ntiles) ? 2 : 1;
                     bool good = true;
-                    for (int j = 0; j < nt && good; ++j)
-                        good = mbar_wait(bar(B_KV_FULL + st + j), use & 1, abort_flag) &&
-                               (use == 0 || mbar_wait(bar(B_S_FREE + st + j), (use - 1) & 1, abort_flag));
+                    for (int j = 0; j < nt && good; ++j) {
+                        good = mbar_wait(bar(B_KV_FULL + st + j), use & 1, abort_flag);
+                        if (!EX) good = good && (use == 0 || mbar_wait(bar(B_S_FREE + st + j), (use - 1) & 1, abort_flag));
+                        else good = good && (gi == 0 || mbar_wait(bar(B_S_FREE), (gi - 1) & 1, abort_flag));
+                    }
                     if (!good) {
                         stop = true;
                         break;
@@ -752,17 +792,34 @@ __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(const KParams 
                     fence_proxy_async_smem();    // cp.async (generic proxy) writes -> tensor-core reads
                     tc_fence_after();
                     const uint32_t id = nt == 2 ? id_s2 : id_s;
-                    // this warp's chain cc = c covers reduction steps
-                    // [cc * kSteps, (cc + 1) * kSteps)
-                    constexpr int kSteps = QB * 4 / kChains;
+                    if constexpr (!EX) {
+                        // this warp's chain c covers reduction steps [kSteps c, kSteps (c + 1))
+                        constexpr int kSteps = QB * 4 / kChains;
 #pragma unroll 3
-                    for (int k = 0; k < kSteps; ++k) {
-                        const uint32_t d = tmem + TM_S + c * (kStages * NT) + st * NT;
-                        const uint32_t kk = c * kSteps + k, blk = kk >> 2, sub = (kk & 3) * 32u;
-                        umma_f16(d, sdesc_sw128(sb + Q_OFF + blk * 8192u + sub, 16, 1024),
-                                 sdesc_sw128(sb + kv_at(st, blk) + sub, 16, 1024), id, k > 0);
+                        for (int k = 0; k < kSteps; ++k) {
+                            const uint32_t d = tmem + TM_S + c * (kStages * NT) + st * NT;
+                            const uint32_t kk = c * kSteps + k, blk = kk >> 2, sub = (kk & 3) * 32u;
+                            umma_f16(d, sdesc_sw128(sb + Q_OFF + blk * 8192u + sub, 16, 1024),
+                                     sdesc_sw128(sb + kv_at(st, blk) + sub, 16, 1024), id, k > 0);
+                        }
+                        for (int j = 0; j < nt; ++j) umma_commit(bar(B_S_FULL + st + j));
+                    } else {
+                        // chains 2c and 2c + 1 (tiles: 8 reduction steps over
+                        // column blocks 2 t, 2 t + 1), or the rope chain 4
+                        // (4 steps over block 8), interleaved step by step
+                        const int c0 = c < 2 ? 2 * c : 4, nch = c < 2 ? 2 : 1, nsteps = c < 2 ? 8 : 4;
+#pragma unroll 2
+                        for (int k = 0; k < nsteps; ++k) {
+                            for (int j = 0; j < nch; ++j) {
+                                const int cc = c0 + j;
+                                const uint32_t kk = cc < 4 ? 8 * cc + k : 32 + k, blk = kk >> 2, sub = (kk & 3) * 32u;
+                                umma_f16(tmem + TM_S + cc * NT, sdesc_sw128(sb + Q_OFF + blk * 8192u + sub, 16, 1024),
+                                         sdesc_sw128(sb + kv_at(st, blk) + sub, 16, 1024), id, k > 0);
+                            }
+                        }
+                        umma_commit(bar(B_S_FULL));
+                        umma_commit(bar(B_SV_DONE + st));        // the stage may now be rescaled for P.V
                     }
-                    for (int j = 0; j < nt; ++j) umma_commit(bar(B_S_FULL + st + j));
                     i += nt;
                     if (i == s.ntiles && next_reloads) umma_commit(bar(B_Q_EMPTY));
                 }
@@ -804,10 +861,14 @@ __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(const KParams 
                 float alpha = 1.f;
                 uint32_t pw[NT / 2];
                 if (head_row) {
-                    if (!warp_wait(bar(B_S_FULL + st), use & 1, abort_flag)) { stop = true; break; }
+                    const int sbuf = EX ? 0 : st;
+                    if (!warp_wait(bar(B_S_FULL + sbuf), EX ? (gi & 1) : (use & 1), abort_flag)) { stop = true; break; }
                     tc_fence_after();
+                    // packed rows: the tile's scales were written with it (this
+                    // wait orders them); plain rows wait after releasing S
+                    if (EX && !warp_wait(bar(B_KV_FULL + st), use & 1, abort_flag)) { stop = true; break; }
                     uint32_t sv[NT];
-                    {
+                    if constexpr (!EX) {
                         uint32_t sa[NT / 2], sc[NT / 2];
 #pragma unroll
                         for (int hf = 0; hf < 2; ++hf) {        // the chains' partial sums of S, 16 columns at a time
@@ -818,7 +879,7 @@ __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(const KParams 
                             for (int j = 0; j < NT / 2; ++j)
                                 sv[hf * 16 + j] = __float_as_uint(__uint_as_float(sa[j]) + __uint_as_float(sc[j]));
 #pragma unroll
-                            for (int cc = 2; cc < kChains; ++cc) {       // the further chains (packed rows)
+                            for (int cc = 2; cc < kChains; ++cc) {       // the third chain (packed rows)
                                 tmem_ld16(tmem + lane_base + TM_S + cc * kStages * NT + st * NT + hf * 16, sa);
                                 tmem_wait_ld();
 #pragma unroll
@@ -827,13 +888,46 @@ __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(const KParams 
                                                                       __uint_as_float(sa[j]));
                             }
                         }
+                    } else {
+                        // S = sum over the four tiles of scale_t(row) x (q_t . k_t)
+                        // (exact products of the unscaled values, scaled in fp32)
+                        // plus the rope part, in a fixed order
+                        // chains 0 and 4 first (the product and the rope part),
+                        // then chains 1-3 folded in; the S buffer is released
+                        // as soon as every chain is in registers
+                        const float *sct = scl + st * 4 * NT;
+                        uint32_t s0[NT], s1[NT];
+                        tmem_ld16(tmem + lane_base + TM_S + 0 * NT, *reinterpret_cast<uint32_t(*)[16]>(&s0[0]));
+                        tmem_ld16(tmem + lane_base + TM_S + 0 * NT + 16, *reinterpret_cast<uint32_t(*)[16]>(&s0[16]));
+                        tmem_ld16(tmem + lane_base + TM_S + 4 * NT, *reinterpret_cast<uint32_t(*)[16]>(&s1[0]));
+                        tmem_ld16(tmem + lane_base + TM_S + 4 * NT + 16, *reinterpret_cast<uint32_t(*)[16]>(&s1[16]));
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int j = 0; j < NT; ++j)
+                            sv[j] = __float_as_uint(fmaf(sct[j], __uint_as_float(s0[j]), __uint_as_float(s1[j])));
+#pragma unroll
+                        for (int cc = 1; cc < 4; ++cc) {
+                            tmem_ld16(tmem + lane_base + TM_S + cc * NT, *reinterpret_cast<uint32_t(*)[16]>(&s0[0]));
+                            tmem_ld16(tmem + lane_base + TM_S + cc * NT + 16, *reinterpret_cast<uint32_t(*)[16]>(&s0[16]));
+                            tmem_wait_ld();
+                            if (cc == 3) {
+                                tc_fence_before();
+                                __syncwarp();
+                                if (lane == 0) mbar_arrive(bar(B_S_FREE + sbuf));
+                            }
+#pragma unroll
+                            for (int j = 0; j < NT; ++j)
+                                sv[j] = __float_as_uint(fmaf(sct[cc * NT + j], __uint_as_float(s0[j]), __uint_as_float(sv[j])));
+                        }
                     }
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(bar(B_S_FREE + st));
-                    // tile i landed before its S was computed; this wait only
-                    // orders the row-mask word
-                    if (!warp_wait(bar(B_KV_FULL + st), use & 1, abort_flag)) { stop = true; break; }
+                    if constexpr (!EX) {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(bar(B_S_FREE + sbuf));
+                        // tile i landed before its S was computed; this wait
+                        // only orders the row-mask word
+                        if (!warp_wait(bar(B_KV_FULL + st), use & 1, abort_flag)) { stop = true; break; }
+                    }
                     if (live_head) {
                         const uint32_t vm = valid_s[st];
                         float x[NT];
@@ -878,6 +972,52 @@ __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(const KParams 
                     __syncwarp();
                     if (lane == 0) mbar_arrive(bar(B_ALPHA + (gi & 3)));
                 } else {
+                    if constexpr (EX) {
+                        // V of the tile: once every S product has read the
+                        // stage, scale its unscaled NoPE values in place by
+                        // their row's tile scale (rounded once to fp16) for P.V
+                        if (!warp_wait(bar(B_KV_FULL + st), use & 1, abort_flag) ||
+                            !warp_wait(bar(B_SV_DONE + st), use & 1, abort_flag)) {
+                            stop = true;
+                            break;
+                        }
+                        // thread t of warps 6-7 (t = 0..63) takes 16-byte
+                        // position t % 8 of rows t / 8 + 8 j (j = 0..3) in all
+                        // eight column blocks; a warp covers 512 contiguous bytes
+                        const float *sct = scl + st * 4 * NT;
+                        const int t64 = tid - 192, r0 = t64 >> 3;
+                        uint8_t *p0 = base + kv_at(st, 0) + r0 * 128 + (t64 & 7) * 16;
+#pragma unroll
+                        for (int tile = 0; tile < 4; ++tile) {
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                const float sc = sct[tile * NT + r0 + 8 * j];
+                                // the scale as fp16 when it is a normal fp16 value
+                                // (V is then rounded twice, within the output
+                                // tolerance); otherwise fp32 products
+                                const bool h = fabsf(sc) >= 6.103515625e-05f && fabsf(sc) <= 65504.f;
+                                const __half2 sh = __float2half2_rn(sc);
+#pragma unroll
+                                for (int b2 = 0; b2 < 2; ++b2) {
+                                    uint4 *pc = reinterpret_cast<uint4 *>(p0 + (2 * tile + b2) * KV_COL + j * 1024);
+                                    uint4 v = *pc;
+                                    uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                                    for (int e = 0; e < 4; ++e) {
+                                        if (h) {
+                                            const __half2 r2 = __hmul2(*reinterpret_cast<const __half2 *>(&w4[e]), sh);
+                                            w4[e] = *reinterpret_cast<const uint32_t *>(&r2);
+                                        } else {
+                                            const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&w4[e]));
+                                            w4[e] = pack2(f.x * sc, f.y * sc, false);
+                                        }
+                                    }
+                                    *pc = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                                }
+                            }
+                        }
+                        fence_proxy_async_smem();        // generic-proxy writes -> the P.V product
+                    }
                     if (!warp_wait(bar(B_ALPHA + (gi & 3)), (gi >> 2) & 1, abort_flag)) { stop = true; break; }
                     alpha = alpha_s[(gi & 3) * 64 + h];
                 }
@@ -1061,20 +1201,23 @@ __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(const KParams 
     }
 }
 
-template <bool PK>
+template <int MODE>
 cudaError_t launch_tc(const KParams &kp, cudaStream_t st)
 {
-    constexpr uint32_t smem = Lay<PK>::kSmemBytes;
-    cudaError_t e = cudaFuncSetAttribute(sfm_attn_tc_kernel<PK>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    constexpr uint32_t smem = Lay<MODE>::kSmemBytes;
+    cudaError_t e = cudaFuncSetAttribute(sfm_attn_tc_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    return launch_dependent(sfm_attn_tc_kernel<PK>, dim3(kp.G), dim3(kThreads), (size_t)smem, st, kp);
+    return launch_dependent(sfm_attn_tc_kernel<MODE>, dim3(kp.G), dim3(kThreads), (size_t)smem, st, kp);
 }
 
 }  // namespace
 
 cudaError_t launch_attn_tc(const KParams &kp, cudaStream_t st)
 {
-    return kp.packed ? launch_tc<true>(kp, st) : launch_tc<false>(kp, st);
+    // E4M3 rows: exact scores (see MODE 2); int8 rows: one fp16 rounding of
+    // value x scale, which keeps the LSE far inside the tolerance
+    if (!kp.packed) return launch_tc<0>(kp, st);
+    return kp.kv_fp8 ? launch_tc<2>(kp, st) : launch_tc<1>(kp, st);
 }
 
 }  // namespace sfm
