@@ -54,6 +54,9 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-second", action="store_true",
                     help="skip the HCA decode block that follows the CSA decode headline")
+    ap.add_argument("--compact-pool", action="store_true",
+                    help="HCA decode: store only the paged blocks the window reads (same attended rows and bytes; "
+                         "a small device footprint for profiler captures)")
     ap.add_argument("--batch", type=int, default=None,
                     help="override the workload's batch size (small-batch measurements; not the headline)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -168,9 +171,11 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # workload accounting (algorithmic bytes / FLOPs)
 # ---------------------------------------------------------------------------
-def make_problem(workload, device, seed, batch=None):
+def make_problem(workload, device, seed, batch=None, compact_pool=False):
     import sfm_inputs as S
     kw = {} if batch is None or workload in ("swa_decode_tiny", "csa_prefill") else {"batch": batch}
+    if compact_pool and workload == "hca_decode":
+        kw["compact_pool"] = True
     return S.WORKLOADS[workload](device=device, seed=seed, **kw)
 
 
@@ -263,13 +268,13 @@ def measured_peaks():
 def make_sets(args, workload, sfm, dev, rank, nsets):
     """Seeded input sets of a workload (enough that their attended bytes
     exceed 3x L2 when nsets is 0), their accounting and per-set buffers."""
-    sets = [make_problem(workload, dev, 1000 + 97 * rank, args.batch)]
+    sets = [make_problem(workload, dev, 1000 + 97 * rank, args.batch, args.compact_pool)]
     acc = [accounting(sets[0], sfm)]
     if nsets <= 0:
         l2 = torch.cuda.get_device_properties(dev).L2_cache_size
         nsets = max(2, min(16, -(-3 * l2 // max(1, acc[0]["bytes"]))))
     for i in range(1, nsets):
-        sets.append(make_problem(workload, dev, 1000 + 97 * rank + i, args.batch))
+        sets.append(make_problem(workload, dev, 1000 + 97 * rank + i, args.batch, args.compact_pool))
         acc.append(accounting(sets[-1], sfm))
     runners = []
     for p in sets:

@@ -224,6 +224,23 @@ def sample_sorted_subsets(counts: torch.Tensor, k: int, g: torch.Generator) -> t
     return out
 
 
+def _block_table_tail(lengths: Sequence[int], bs: int, tail: int, g: torch.Generator, device):
+    """Block table that stores only the last `tail` logical blocks of each
+    sequence (in a random permutation of physical blocks 1..); every other
+    logical block maps to physical block 0, which holds no row any query
+    reads.  For workloads whose queries read only the end of each sequence."""
+    nblk = [max(1, math.ceil(int(L) / bs)) for L in lengths]
+    keep = [min(tail, n) for n in nblk]
+    total = 1 + sum(keep)
+    perm = (torch.randperm(total - 1, generator=g, device=device) + 1).to(torch.int32)
+    table = torch.zeros(len(lengths), max(nblk), dtype=torch.int32, device=device)
+    o = 0
+    for b, (n, k) in enumerate(zip(nblk, keep)):
+        table[b, n - k:n] = perm[o:o + k]
+        o += k
+    return table, total
+
+
 def _block_table(lengths: Sequence[int], bs: int, g: torch.Generator, device, min_cols: int = 1):
     nblk = [max(1, math.ceil(int(L) / bs)) for L in lengths]
     total = sum(nblk)
@@ -251,7 +268,8 @@ def build(name: str, *, seed: int, device="cpu", q_n: int, q_lens: Sequence[int]
           kv_capacity: Optional[int] = None, seqused_q: Optional[Sequence[int]] = None,
           pass_seqused_ori: Optional[bool] = None, pass_seqused_cmp: Optional[bool] = None,
           residuals: Optional[Sequence[int]] = None, cmp_lens: Optional[Sequence[int]] = None,
-          index_mode: str = "visible", kv_row_pad: int = 0, sparse_block_size: int = 1) -> Problem:
+          index_mode: str = "visible", kv_row_pad: int = 0, sparse_block_size: int = 1,
+          ori_tail_blocks: Optional[int] = None) -> Problem:
     """Build a problem.
 
     mode: 'swa' (ori window only), 'csa' (window + top-k compressed),
@@ -263,6 +281,10 @@ def build(name: str, *, seed: int, device="cpu", q_n: int, q_lens: Sequence[int]
     kv_row_pad: extra bytes between consecutive KV rows (inter-row padding).
     sparse_block_size: 'ori_sparse' only; each index selects a block of that
           many tokens (sampled among the blocks holding a visible token).
+    ori_tail_blocks: PAGED ori caches only: store just the last that many
+          blocks of each sequence (the rest of the block table points at one
+          shared block no query reads) -- a small device footprint for
+          workloads that read only the end of each sequence.
     """
     assert layout_q in LAYOUTS_Q and layout_kv in LAYOUTS_KV
     B = len(q_lens)
@@ -315,12 +337,15 @@ def build(name: str, *, seed: int, device="cpu", q_n: int, q_lens: Sequence[int]
         t["seqused_q"] = torch.tensor(list(seqused_q), dtype=torch.int32, device=device)
 
     # ---------------- caches ----------------
-    def make_cache(lengths, bs, capacity):
+    def make_cache(lengths, bs, capacity, tail=None):
         row_bytes = (PACKED_ROW_BYTES if rope_head_dim == 64 else PACKED_ROW_BYTES_ROPE0) if packed else d_v * 2
         stride_bytes = row_bytes + kv_row_pad
         table = None
         if layout_kv == "PAGED":
-            table, nblk = _block_table(lengths, bs, g, device)
+            if tail is not None:
+                table, nblk = _block_table_tail(lengths, bs, tail, g, device)
+            else:
+                table, nblk = _block_table(lengths, bs, g, device)
             nrows = nblk * bs
             shape = (nblk, bs, 1)
         elif layout_kv == "TND":
@@ -346,7 +371,7 @@ def build(name: str, *, seed: int, device="cpu", q_n: int, q_lens: Sequence[int]
             cache = raw.view(tdt).view(*shape, d_v)
         return cache, table, stride_bytes
 
-    ori_kv, ori_table, ori_stride = make_cache(kv_lens, ori_block_size, kv_capacity)
+    ori_kv, ori_table, ori_stride = make_cache(kv_lens, ori_block_size, kv_capacity, ori_tail_blocks)
     t["ori_kv"] = ori_kv
     t["ori_block_table"] = ori_table
     if layout_kv == "TND":
@@ -484,12 +509,15 @@ def csa_decode(device="cpu", seed: int = 1, batch: int = 32, cmp_topk: int = 512
                  win_left=127, win_right=0, sinks=True, return_lse=True)
 
 
-def hca_decode(device="cpu", seed: int = 2, batch: int = 64, kv_len: int = 131072) -> Problem:
+def hca_decode(device="cpu", seed: int = 2, batch: int = 64, kv_len: int = 131072, compact_pool: bool = False) -> Problem:
     """HCA decode: q_n=128, paged ori (block 128) with kv_len=131072, window
-    127/0, cmp_ratio 128 with all 1024 visible slots, fp32 sinks."""
+    127/0, cmp_ratio 128 with all 1024 visible slots, fp32 sinks.
+    compact_pool stores only the two last ori blocks of each sequence (the
+    window reads nothing else): the same attended rows and bytes in a small
+    device footprint (for profiler captures)."""
     return build("hca_decode", seed=seed, device=device, q_n=128, q_lens=[1] * batch, kv_lens=[kv_len] * batch,
                  layout_q="BSND", layout_kv="PAGED", mode="hca", cmp_ratio=128, win_left=127, win_right=0,
-                 sinks=True, return_lse=True)
+                 sinks=True, return_lse=True, ori_tail_blocks=2 if compact_pool else None)
 
 
 def csa_prefill(device="cpu", seed: int = 3, nseq: int = 8, qmin: int = 512, qmax: int = 4096,

@@ -134,6 +134,7 @@ REDUCED = {
     "swa_decode_tiny": lambda: S.swa_decode_tiny(device="cuda"),
     "csa_decode_b4": lambda: S.csa_decode(device="cuda", batch=4),
     "hca_decode_b2": lambda: S.hca_decode(device="cuda", batch=2),
+    "hca_decode_b2_compact_pool": lambda: S.hca_decode(device="cuda", batch=2, compact_pool=True),
     "csa_prefill_small": lambda: S.csa_prefill(device="cuda", nseq=3, qmin=40, qmax=300, prefix_max=700),
     "packed_decode_b3": lambda: S.packed_decode(device="cuda", batch=3, kv_len=8192),
 }
