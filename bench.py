@@ -59,6 +59,10 @@ def parse():
                          "a small device footprint for profiler captures)")
     ap.add_argument("--batch", type=int, default=None,
                     help="override the workload's batch size (small-batch measurements; not the headline)")
+    ap.add_argument("--split-policy", choices=("invariant", "occupancy"), default="invariant",
+                    help="sfm_params.split_policy: batch-invariant splits (the default) or occupancy splits")
+    ap.add_argument("--no-small-batch", action="store_true",
+                    help="skip the small-batch block (CSA / HCA decode at B = 4, 8, 16 under both split policies)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     return ap.parse_args()
 
@@ -277,8 +281,9 @@ def make_sets(args, workload, sfm, dev, rank, nsets):
         sets.append(make_problem(workload, dev, 1000 + 97 * rank + i, args.batch, args.compact_pool))
         acc.append(accounting(sets[-1], sfm))
     runners = []
+    policy = sfm.SPLIT_OCCUPANCY if args.split_policy == "occupancy" else sfm.SPLIT_BATCH_INVARIANT
     for p in sets:
-        params = sfm.make_params(**p.attrs())
+        params = sfm.make_params(**p.attrs(), split_policy=policy)
         tens = sfm.make_tensors(p.t["q"], p.t["ori_kv"], **p.tensor_kwargs())
         md = torch.empty(sfm.sfm_metadata_size(params), dtype=torch.int32, device=dev)
         nb = sfm.sfm_workspace_size(params)
@@ -308,6 +313,8 @@ def measure(args, workload, sfm, dev, rank, world, sampler, nsets):
     torch.cuda.synchronize()
     if int(status.item()) != 0:
         raise RuntimeError(f"{workload}: device status {int(status.item()):#x} during warm-up")
+    # work units of the first set's plan: splits (header word 6) x head groups
+    units = int(runners[0][3][6].item()) * ((sets[0].num_heads_q + 63) // 64)
 
     # kernels per step: the planner, the attention kernel and, when a row can
     # have more than one split (a split-KV workspace is needed), the combine
@@ -404,6 +411,7 @@ def measure(args, workload, sfm, dev, rank, world, sampler, nsets):
         "step": "sfm_metadata (device planner) + sfm_forward (attention"
                 + (" + split combine)" if launches_per_step == 3 else "; one split per row, no combine)"),
         "parallelism": f"replicas x{world}",
+        "split_policy": args.split_policy, "work_units": units,
     }
     res = {
         "workload": workload, "K": K, "W": W, "ms_max": ms_max, "rows_total": rows_total,
@@ -443,6 +451,26 @@ def run_ours(args):
         second, s2, _ = measure(args, "hca_decode", sfm, dev, rank, world, sampler, 0)
         del s2
         torch.cuda.empty_cache()
+    # small decode batches under both split policies (compact pools: the same
+    # attended rows, a small footprint)
+    small = None
+    if args.workload == "csa_decode" and args.batch is None and not args.no_small_batch:
+        small = {}
+        for wl in ("csa_decode", "hca_decode"):
+            for B in (4, 8, 16):
+                for pol in ("invariant", "occupancy"):
+                    a = argparse.Namespace(**vars(args))
+                    a.batch, a.compact_pool, a.split_policy, a.sets = B, True, pol, 0
+                    a.steps, a.warmup = min(args.steps, 100), max(3, min(args.warmup, 10))
+                    r, s3, _ = measure(a, wl, sfm, dev, rank, world, sampler, 0)
+                    del s3
+                    small.setdefault(wl, {}).setdefault(str(B), {})[pol] = {
+                        "ms_per_step": r["ms_max"] / r["K"], "kernel_ms": r["roofline"]["kernel_ms_avg"],
+                        "forward_only_ms_per_step": r["fwd_ms"] / r["K"], "work_units": r["config"]["work_units"],
+                        "value": r["rows_total"] / (r["ms_max"] * 1e-3), "steps": r["K"],
+                        "launches": r["launches_per_step"] * r["K"], "clocks_sm_mhz": r["clocks"].get("sm_mhz"),
+                    }
+        torch.cuda.empty_cache()
     sampler.stop()
 
     ms_max = head["ms_max"]
@@ -478,7 +506,9 @@ def run_ours(args):
                                      "combine) on plans made beforehand, "
                                      "as a model reuses one plan across its layers"},
             "gpu_launches": head["launches_per_step"] * K + (second["launches_per_step"] * second["K"]
-                                                             if second else 0),
+                                                             if second else 0)
+                            + (sum(v["launches"] for w in small.values() for b in w.values() for v in b.values())
+                               if small else 0),
             "clocks": head["clocks"],
         }
         if second:
@@ -490,6 +520,14 @@ def run_ours(args):
                 "roofline": second["roofline"], "config": second["config"], "clocks": second["clocks"],
                 "note": "the second configuration of the >= 70 % roofline target, timed in the same run "
                         "after the headline (its launches are counted in gpu_launches)",
+            }
+        if small:
+            line["small_batch"] = {
+                **small,
+                "unit": "tokens/s", "n_gpus_per_rank": 1,
+                "note": "decode batches of 4, 8 and 16 rows, timed like the headline (planner + forward per "
+                        "step) under the batch-invariant split policy (the default) and the occupancy policy; "
+                        "launches counted in gpu_launches",
             }
         print(json.dumps(line))
     if world > 1:
@@ -519,7 +557,7 @@ def run_e2e(args, sfm, sets, acc, dev, stream):
             layout_kv=p.layout_kv, has_cmp_kv=p.has_cmp_kv, dtype=p.torch_dtype,
             kv_format=S_KV_FORMAT_CODES[p.kv_format], rope_head_dim=p.rope_head_dim,
             ori_block_size=p.ori_block_size, cmp_block_size=p.cmp_block_size, return_softmax_lse=True,
-            device=dev, stream=st)
+            batch_invariant=args.split_policy == "invariant", device=dev, stream=st)
         sfm.sparse_flash_mla(
             T["q"], metadata=md, ori_kv=T["ori_kv"], cmp_kv=T["cmp_kv"], ori_sparse_indices=T["ori_sparse_indices"],
             cmp_sparse_indices=T["cmp_sparse_indices"], ori_block_table=T["ori_block_table"],

@@ -62,7 +62,7 @@
 extern "C" {
 #endif
 
-#define SFM_ABI_VERSION 3
+#define SFM_ABI_VERSION 4
 
 /* A cudaStream_t, passed as an untyped pointer so this header needs no CUDA headers. */
 typedef void *sfm_stream_t;
@@ -89,6 +89,22 @@ enum sfm_dtype { SFM_DTYPE_BF16 = 0, SFM_DTYPE_FP16 = 1 };
  *                       7, 3 mantissa bits, no infinity, S.1111.111 = NaN):
  *                       K~[d] = e4m3(byte d) * scale[d / 128]. */
 enum sfm_kv_format { SFM_KV_PLAIN = 0, SFM_KV_INT8_PACKED = 1, SFM_KV_FP8_PACKED = 2 };
+
+/* How sfm_metadata sizes the split-KV chunks of a query row ("sparse_flash_mla"
+ * doc, 确定性计算: deterministic results and batch invariance are the default).
+ *   SFM_SPLIT_BATCH_INVARIANT  a row is cut into chunks whose size depends
+ *       only on the head count and the query shape (max_seqlen_q): a row's O
+ *       and LSE are bit for bit the same whatever other rows share the batch
+ *       and however many there are.  Batches much smaller than one row per
+ *       SM leave SMs idle (a 128-head row of 1152 positions is two work
+ *       units, so 8 such rows keep 16 SMs busy).
+ *   SFM_SPLIT_OCCUPANCY        where the batch-invariant plan has fewer work
+ *       units than the kernel has CTAs, the chunk size is chosen from the
+ *       number of query rows and the SM count as well, so the units fill the
+ *       SMs; otherwise the plan is the batch-invariant one.  Results are
+ *       deterministic for given params and lengths, but a row's rounding can
+ *       change with the batch size. */
+enum sfm_split_policy { SFM_SPLIT_BATCH_INVARIANT = 0, SFM_SPLIT_OCCUPANCY = 1 };
 
 /* Host-side return codes. */
 enum sfm_error {
@@ -151,6 +167,7 @@ typedef struct sfm_params {
                                   each still under the ori mask ([QSFA] / [SFA] 属性参数:
                                   sparse_block_size; the tokens of a block share the
                                   selection decision) */
+    int32_t split_policy;      /* enum sfm_split_policy (0 = batch invariant) */
 } sfm_params;
 
 /* Device tensors of one call.  Shapes (row = one KV row of row_stride bytes):

@@ -31,6 +31,7 @@ LIB_PATH = os.path.join(_HERE, "_build", "libsfm.so")
 BSND, TND, PAGED = 0, 1, 2
 BF16, FP16 = 0, 1
 KV_PLAIN, KV_INT8_PACKED, KV_FP8_PACKED = 0, 1, 2
+SPLIT_BATCH_INVARIANT, SPLIT_OCCUPANCY = 0, 1
 _LAYOUTS = {"BSND": BSND, "TND": TND, "PAGED": PAGED, "PA_BBND": PAGED, "PA_BSND": PAGED, "PA_ND": PAGED}
 
 STATUS_BAD_INDEX = 0x01
@@ -46,7 +47,8 @@ class SfmParams(C.Structure):
         "num_heads_q", "num_heads_kv", "head_dim", "rope_head_dim", "batch_size", "max_seqlen_q", "total_q",
         "max_seqlen_ori_kv", "max_seqlen_cmp_kv", "ori_topk", "cmp_topk", "cmp_ratio", "ori_mask_mode",
         "cmp_mask_mode", "ori_win_left", "ori_win_right", "layout_q", "layout_kv", "has_ori_kv", "has_cmp_kv",
-        "dtype", "kv_format", "ori_block_size", "cmp_block_size", "return_lse", "kernel_hint", "sparse_block_size")]
+        "dtype", "kv_format", "ori_block_size", "cmp_block_size", "return_lse", "kernel_hint", "sparse_block_size",
+        "split_policy")]
 
     def as_dict(self):
         return {n: getattr(self, n) for n, _ in self._fields_}
@@ -258,7 +260,8 @@ def make_params(**kw) -> SfmParams:
     defaults = dict(num_heads_kv=1, head_dim=512, rope_head_dim=0, total_q=0, max_seqlen_cmp_kv=0, ori_topk=0,
                     cmp_topk=0, cmp_ratio=1, ori_mask_mode=4, cmp_mask_mode=3, ori_win_left=-1, ori_win_right=-1,
                     layout_q=BSND, layout_kv=BSND, has_ori_kv=1, has_cmp_kv=0, dtype=BF16, kv_format=KV_PLAIN,
-                    ori_block_size=0, cmp_block_size=0, return_lse=0, kernel_hint=0, sparse_block_size=1)
+                    ori_block_size=0, cmp_block_size=0, return_lse=0, kernel_hint=0, sparse_block_size=1,
+                    split_policy=SPLIT_BATCH_INVARIANT)
     defaults.update(kw)
     for k, v in defaults.items():
         if k in ("layout_q", "layout_kv") and isinstance(v, str):
@@ -287,8 +290,13 @@ def sparse_flash_mla_metadata(num_heads_q: int, num_heads_kv: int, head_dim: int
                               ori_win_right=-1, layout_q="BSND", layout_kv="BSND", has_ori_kv=True,
                               has_cmp_kv=True, dtype=torch.bfloat16, kv_format=KV_PLAIN, rope_head_dim=0,
                               ori_block_size=0, cmp_block_size=0, return_softmax_lse=False,
-                              sparse_block_size=1, device=None, stream=None) -> Metadata:
-    """Enqueue the device planner and return its plan (two-call contract)."""
+                              sparse_block_size=1, batch_invariant=True, device=None,
+                              stream=None) -> Metadata:
+    """Enqueue the device planner and return its plan (two-call contract).
+
+    ``batch_invariant=False`` selects the occupancy split policy: small
+    batches are cut into more chunks so they fill the SMs, at the price of a
+    row's rounding depending on the batch size."""
     if layout_q == "TND" and cu_seqlens_q is not None:
         batch_size = cu_seqlens_q.numel() - 1
     params = make_params(
@@ -298,7 +306,8 @@ def sparse_flash_mla_metadata(num_heads_q: int, num_heads_kv: int, head_dim: int
         ori_mask_mode=ori_mask_mode, cmp_mask_mode=cmp_mask_mode, ori_win_left=ori_win_left,
         ori_win_right=ori_win_right, layout_q=layout_q, layout_kv=layout_kv, has_ori_kv=int(has_ori_kv),
         has_cmp_kv=int(has_cmp_kv), dtype=dtype, kv_format=kv_format, ori_block_size=ori_block_size,
-        cmp_block_size=cmp_block_size, return_lse=int(return_softmax_lse), sparse_block_size=sparse_block_size)
+        cmp_block_size=cmp_block_size, return_lse=int(return_softmax_lse), sparse_block_size=sparse_block_size,
+        split_policy=SPLIT_BATCH_INVARIANT if batch_invariant else SPLIT_OCCUPANCY)
     lengths = make_tensors(None, None, cu_seqlens_q=cu_seqlens_q, cu_seqlens_ori_kv=cu_seqlens_ori_kv,
                            cu_seqlens_cmp_kv=cu_seqlens_cmp_kv, seqused_q=seqused_q, seqused_ori_kv=seqused_ori_kv,
                            seqused_cmp_kv=seqused_cmp_kv, cmp_residual_kv=cmp_residual_kv, ori_row_stride=0)

@@ -87,6 +87,8 @@ int validate_params(const sfm_params *pp)
     if (p.return_lse != 0 && p.return_lse != 1) return SFM_ERR_INVALID_ARG;
     if (p.kernel_hint < 0 || p.kernel_hint > 2) return SFM_ERR_INVALID_ARG;
     if (p.kernel_hint == 1) return SFM_ERR_UNSUPPORTED;   // the CUDA-core kernel is retired
+    if (p.split_policy != SFM_SPLIT_BATCH_INVARIANT && p.split_policy != SFM_SPLIT_OCCUPANCY)
+        return SFM_ERR_INVALID_ARG;
     return SFM_OK;
 }
 
@@ -138,6 +140,40 @@ struct Plan {
     int64_t T, max_splits_per_token;
 };
 
+int head_groups(const sfm_params &p) { return (p.num_heads_q + 63) / 64; }
+
+// Occupancy policy: when the batch-invariant plan leaves CTAs without a work
+// unit, re-cut every row into k chunks, k chosen by a cost model of the step,
+// in half-tiles.  A CTA runs ceil(units / G) units one after the other; a
+// unit costs its 32-row tiles, at least three (shorter units hide behind the
+// kernel's start-up), plus one tile of epilogue; splitting a row adds the
+// combine launch (one tile) and half a tile per chunk of the row to merge.
+// Fitted to decode steps timed on one GPU with 64 and 128 heads at 4 to 16
+// rows.  The model is evaluated on the params' upper bound of a row's
+// positions, so the plan still does not depend on the lengths.
+void occupancy_split(const sfm_params &p, Plan *pl, int64_t mp)
+{
+    const int64_t hg = head_groups(p);
+    const int64_t units_inv = pl->T * hg * pl->max_splits_per_token;
+    if (pl->T <= 0 || mp <= 0 || units_inv >= pl->G) return;
+    const int64_t tiles = (mp + 31) / 32;
+    auto cost = [&](int64_t k) {
+        const int64_t waves = (pl->T * hg * k + pl->G - 1) / pl->G;
+        const int64_t per_unit = (tiles + k - 1) / k;
+        return 2 * waves * ((per_unit > 3 ? per_unit : 3) + 1) + (k > 1 ? 2 + k : 0);
+    };
+    int64_t best_k = pl->max_splits_per_token, best = cost(best_k);
+    const int64_t kmax = tiles < pl->G ? tiles : pl->G;     // more chunks than CTAs only adds waves
+    for (int64_t k = best_k + 1; k <= kmax; ++k) {
+        const int64_t c = cost(k);
+        if (c < best) best = c, best_k = k;
+    }
+    if (best_k == pl->max_splits_per_token) return;
+    const int64_t rows = 32 * ((tiles + best_k - 1) / best_k);
+    pl->split_rows = (int32_t)rows;
+    pl->max_splits_per_token = (mp + rows - 1) / rows;
+}
+
 // Split size: decode-shaped calls (few query rows per sequence) cut each
 // row's attended positions into fixed chunks so the SMs share the work;
 // prefill-shaped calls have enough rows and keep one split per row.  The
@@ -165,11 +201,13 @@ int make_plan(const sfm_params &p, Plan *pl)
     // packed decode, 64 rows of at most 2048 positions: one split per row,
     // 128 units, no partials to merge).  Measured on one GPU against
     // 768-row splits: HCA decode step -13 %, packed decode -8 %.  Batches of
-    // fewer rows leave SMs idle.
+    // fewer rows leave SMs idle unless the params ask for the occupancy
+    // policy, which re-cuts the rows so the units fill the SMs.
     const int split = p.num_heads_q > 64 ? 2048 : 160;
     pl->split_rows = decode_like ? split : (1 << 30);
     const int64_t mp = max_positions(p);
     pl->max_splits_per_token = decode_like ? (mp + pl->split_rows - 1) / pl->split_rows : 1;
+    if (p.split_policy == SFM_SPLIT_OCCUPANCY) occupancy_split(p, pl, mp);
     return SFM_OK;
 }
 
@@ -197,7 +235,6 @@ size_t ws_lse_offset(const sfm_params &p, int64_t cap)
     return (o + 255) & ~(size_t)255;
 }
 
-int head_groups(const sfm_params &p) { return (p.num_heads_q + 63) / 64; }
 
 size_t workspace_bytes_for(const sfm_params &p, const Plan &pl)
 {

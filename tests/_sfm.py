@@ -48,8 +48,8 @@ class Runner:
         return self.out, self.lse, int(self.status.item())
 
 
-def run(prob):
-    return Runner(prob).run()
+def run(prob, params=None):
+    return Runner(prob, params).run()
 
 
 def _dump_cap(prob):
@@ -72,13 +72,13 @@ def _dump_cap(prob):
 UNWRITTEN = -2
 
 
-def debug_rows(prob, cap=None):
+def debug_rows(prob, cap=None, params=None):
     """The KV rows the attention kernel's resolver handed to its copy warps,
     per query row, through sfm_debug_attended (the real forward with its dump
     on).  Returns (entries, out, lse, status): entries[t] is the int32 array
     of positions 0..counts[t]-1 (-1 skipped, r an ori pool row, r | 1 << 31 a
     cmp pool row; UNWRITTEN where the kernel wrote nothing)."""
-    r = Runner(prob)
+    r = Runner(prob, params)
     cap = cap or _dump_cap(prob)
     dev = prob.t["q"].device
     rows = torch.full((prob.num_tokens, cap), UNWRITTEN, dtype=torch.int32, device=dev)

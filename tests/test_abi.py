@@ -32,7 +32,7 @@ def test_header_declares_the_entry_points():
 def test_library_exports_every_declared_symbol(lib):
     for name in declared_functions():
         assert hasattr(lib, name), name
-    assert sfm.sfm_abi_version() == 3
+    assert sfm.sfm_abi_version() == 4
 
 
 def test_error_strings(lib):
@@ -78,6 +78,8 @@ BAD = [
     ("kernel hint 3", dict(kernel_hint=3), 1),
     ("kernel hint 1 (retired CUDA-core kernel)", dict(kernel_hint=1), 2),
     ("kernel hint -1", dict(kernel_hint=-1), 1),
+    ("split policy 2", dict(split_policy=2), 1),
+    ("split policy -1", dict(split_policy=-1), 1),
     ("window right -2", dict(ori_win_right=-2), 1),
     ("paged cmp block 8", dict(layout_kv=sfm.PAGED, ori_block_size=128, has_cmp_kv=1, cmp_ratio=4, cmp_topk=64,
                                cmp_mask_mode=3, cmp_block_size=8), 3),

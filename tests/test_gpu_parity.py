@@ -73,7 +73,7 @@ def _pool_rows(host, t, src, pos):
     return rows
 
 
-def assert_sets(prob, tokens=None, host=None, out=None, lse=None):
+def assert_sets(prob, tokens=None, host=None, out=None, lse=None, params=None):
     """Exact attended sets of the attention kernel itself: the rows its
     resolver handed to the copy warps (sfm_debug_attended), in position
     order, against the oracle's attended set mapped to pool rows; every
@@ -81,7 +81,7 @@ def assert_sets(prob, tokens=None, host=None, out=None, lse=None):
     dump call's outputs must equal them bit for bit (the dump does not change
     the computation)."""
     host = host or prob.to("cpu")
-    entries, o_dbg, l_dbg, status = _sfm.debug_rows(prob)
+    entries, o_dbg, l_dbg, status = _sfm.debug_rows(prob, params=params)
     assert status & ~sfm.STATUS_BAD_INDEX == 0, hex(status)
     if out is not None:
         assert torch.equal(o_dbg, out), f"{prob.name}: output of the dump call differs"
@@ -231,6 +231,61 @@ def test_batch_invariance():
         o1, l1, st = _sfm.run(single)
         assert st == 0
         assert torch.equal(o1[0], out[b]) and torch.equal(l1[0], lse[b]), b
+
+
+# ---------------------------------------------------------------------------
+# occupancy split policy: batches too small to fill the SMs are cut finer
+# ---------------------------------------------------------------------------
+OCCUPANCY = {
+    "csa_decode_b4": lambda: S.csa_decode(device="cuda", batch=4),
+    "hca_decode_b8": lambda: S.hca_decode(device="cuda", batch=8, compact_pool=True),
+    "packed_decode_b3": lambda: S.packed_decode(device="cuda", batch=3, kv_len=8192),
+    "packed_fp8_decode_b2": lambda: S.packed_fp8_decode(device="cuda", batch=2, kv_len=8192),
+}
+
+
+def _units(meta, q_n):
+    m = meta.cpu().numpy()
+    return int(m[6]) * ((q_n + 63) // 64), int(m[4])
+
+
+@pytest.mark.parametrize("key", list(OCCUPANCY))
+def test_occupancy_policy(key):
+    """SFM_SPLIT_OCCUPANCY: the plan of a small batch has more work units than
+    the batch-invariant one (at least 64 for eight 128-head HCA rows, which
+    the batch-invariant plan runs as 16), the outputs match the oracle on
+    every row, the attended sets are exact, and two calls give the same
+    bits."""
+    prob = OCCUPANCY[key]()
+    inv = _sfm.Runner(prob)
+    inv.plan()
+    occ = _sfm.Runner(prob, _sfm.params_of(prob, split_policy=sfm.SPLIT_OCCUPANCY))
+    out, lse, status = occ.run()
+    assert status == 0, hex(status)
+    u_inv, s_inv = _units(inv.meta, prob.num_heads_q)
+    u_occ, s_occ = _units(occ.meta, prob.num_heads_q)
+    assert u_occ > u_inv and s_occ < s_inv, (u_inv, u_occ, s_inv, s_occ)
+    if key == "hca_decode_b8":
+        assert u_inv == 16 and u_occ >= 64, (u_inv, u_occ)
+    out, lse = out.clone(), lse.clone()
+    host = prob.to("cpu")
+    assert_parity(prob, out, lse, host=host)
+    assert_sets(prob, host=host, out=out, lse=lse, params=occ.params)
+    o2, l2, _ = occ.run()
+    assert torch.equal(o2, out) and torch.equal(l2, lse)
+
+
+def test_occupancy_policy_keeps_full_batches_invariant():
+    """Where the batch-invariant plan already gives every CTA a unit, the
+    occupancy policy leaves the plan (and so the bits) unchanged."""
+    prob = S.csa_decode(device="cuda", batch=64, seed=3)
+    a = _sfm.Runner(prob)
+    b = _sfm.Runner(prob, _sfm.params_of(prob, split_policy=sfm.SPLIT_OCCUPANCY))
+    oa, la, sa = a.run()
+    ob, lb, sb = b.run()
+    assert sa == 0 and sb == 0
+    assert _units(a.meta, 64) == _units(b.meta, 64)
+    assert torch.equal(oa, ob) and torch.equal(la, lb)
 
 
 def test_context_parallel_split_on_gpu():

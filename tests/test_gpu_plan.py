@@ -133,6 +133,8 @@ CASES = {
                           mode="csa", cmp_ratio=4, cmp_topk=128, sinks=True),
     "hca_decode_64_heads128": dict(q_n=128, q_lens=[1] * 64, kv_lens=[2000 + 13 * b for b in range(64)],
                                    layout_kv="PAGED", mode="hca", cmp_ratio=128),
+    "hca_decode_8_heads128": dict(q_n=128, q_lens=[1] * 8, kv_lens=[1500 + 977 * b for b in range(8)],
+                                  layout_kv="PAGED", mode="hca", cmp_ratio=128),
     "swa_empty_rows": dict(q_n=16, q_lens=[1] * 6, kv_lens=[0, 500, 0, 1000, 3, 0], layout_kv="PAGED", mode="swa"),
     "causal_many_splits": dict(q_n=64, q_lens=[1, 1, 1, 1], kv_lens=[6000, 100, 1300, 2600], layout_kv="PAGED",
                                mode="swa", ori_mask_mode=3, win_left=-1, win_right=-1),
@@ -158,3 +160,56 @@ def test_plan_words(name):
     torch.cuda.synchronize()
     W, G = check_plan(prob, r.meta, q_n)
     assert G >= 1
+
+
+def _occupancy_split(T, q_n, mp, G, S_inv):
+    """The occupancy policy's chunk size, written out: keep the batch-invariant
+    cut when its units already reach G; otherwise take the k (chunks per row)
+    that minimises 2 waves (max(tiles per chunk, 3) + 1), plus 2 + k when a
+    row is split, the smallest k on ties."""
+    hg = (q_n + 63) // 64
+    ms = -(-mp // S_inv)
+    if T * hg * ms >= G:
+        return S_inv
+    tiles = -(-mp // 32)
+    def cost(k):
+        return 2 * -(-(T * hg * k) // G) * (max(-(-tiles // k), 3) + 1) + (2 + k if k > 1 else 0)
+    best = min(range(ms, min(tiles, G) + 1), key=lambda k: (cost(k), k))
+    return S_inv if best == ms else 32 * -(-tiles // best)
+
+
+def _max_positions(p):
+    """Upper bound of a row's attended positions from the params alone."""
+    if p.ori_topk > 0:
+        ori = p.ori_topk * max(1, p.sparse_block_size)
+    else:
+        ori = p.max_seqlen_ori_kv
+        if p.ori_mask_mode == 4 and p.ori_win_left >= 0 and p.ori_win_right >= 0:
+            ori = min(ori, p.ori_win_left + p.ori_win_right + 1)
+    cmp = (p.cmp_topk if p.cmp_topk > 0 else p.max_seqlen_cmp_kv) if p.has_cmp_kv else 0
+    return ori + cmp
+
+
+OCC_CASES = ["csa_decode_32", "hca_decode_8_heads128", "mtp_q2", "swa_empty_rows", "causal_many_splits",
+             "prefill_tnd"]
+
+
+@pytest.mark.parametrize("name", OCC_CASES)
+def test_plan_words_occupancy_policy(name):
+    """The occupancy policy's plan: the same plan words for its chunk size,
+    the chunk size the policy's cost model picks, and never fewer work units
+    than the batch-invariant plan."""
+    kw = dict(CASES[name])
+    q_n = kw.pop("q_n")
+    prob = S.build(name, seed=71, device="cuda", q_n=q_n, **kw)
+    inv = _sfm.Runner(prob)
+    inv.plan()
+    occ = _sfm.Runner(prob, _sfm.params_of(prob, split_policy=sfm.SPLIT_OCCUPANCY))
+    occ.plan()
+    torch.cuda.synchronize()
+    W_inv, G = check_plan(prob, inv.meta, q_n)
+    W_occ, _ = check_plan(prob, occ.meta, q_n)
+    S_inv, S_occ = int(inv.meta[4]), int(occ.meta[4])
+    mp = _max_positions(occ.params)
+    assert S_occ == _occupancy_split(prob.num_tokens, q_n, mp, G, S_inv), (S_inv, S_occ)
+    assert W_occ >= W_inv
