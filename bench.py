@@ -38,6 +38,7 @@ sys.path.insert(0, ROOT)
 
 import torch  # noqa: E402
 
+NOMINAL_HBM_GBS = 7900.0      # HBM3e, nominal (the measured copy rate is the stricter denominator)
 WORKLOADS = ("csa_decode", "hca_decode", "packed_decode", "packed_fp8_decode", "csa_prefill")
 S_KV_FORMAT_CODES = {"plain": 0, "int8_packed": 1, "fp8_packed": 2}     # sfm_params.kv_format
 
@@ -364,6 +365,54 @@ def measure(args, workload, sfm, dev, rank, world, sampler, nsets):
     f1.record(stream)
     torch.cuda.synchronize()
     fwd_ms = max_over_ranks(f0.elapsed_time(f1), world, dev)
+
+    # the same forwards captured as one CUDA graph of back-to-back calls
+    # (rotating over the sets), replayed: launch cost off the host
+    KG = min(K, 100)
+    graph = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream(device=dev)
+    cap.wait_stream(stream)
+    with torch.cuda.stream(cap):
+        with torch.cuda.graph(graph, stream=cap):
+            cs = torch.cuda.current_stream()
+            for k in range(KG):
+                p, params, tens, md, ws, out, lse = runners[k % len(runners)]
+                sfm.sfm_forward(params, tens, md, p.softmax_scale, out, lse, ws, status, cs)
+    stream.wait_stream(cap)
+    graph.replay()
+    torch.cuda.synchronize()
+    reps = max(1, K // KG)
+    g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    g0.record(stream)
+    for _ in range(reps):
+        graph.replay()
+    g1.record(stream)
+    torch.cuda.synchronize()
+    graph_ms = max_over_ranks(g0.elapsed_time(g1), world, dev) / (reps * KG)
+    del graph
+
+    # L2-warm, labelled: one input set's forward repeated (its KV stays in L2)
+    p, params, tens, md, ws, out, lse = runners[0]
+    for _ in range(W):
+        sfm.sfm_forward(params, tens, md, p.softmax_scale, out, lse, ws, status, stream)
+    torch.cuda.synchronize()
+    w0, w1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    w0.record(stream)
+    for _ in range(K):
+        sfm.sfm_forward(params, tens, md, p.softmax_scale, out, lse, ws, status, stream)
+    w1.record(stream)
+    torch.cuda.synchronize()
+    warm_ms = max_over_ranks(w0.elapsed_time(w1), world, dev) / K
+
+    # the planner alone (sfm_metadata back to back over the sets)
+    m0, m1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    m0.record(stream)
+    for k in range(K):
+        p, params, tens, md, ws, out, lse = runners[k % len(runners)]
+        sfm.sfm_metadata(params, tens, md, stream)
+    m1.record(stream)
+    torch.cuda.synchronize()
+    plan_ms = max_over_ranks(m0.elapsed_time(m1), world, dev) / K
     if int(status.item()) != 0:
         raise RuntimeError(f"{workload}: device status {int(status.item()):#x} during the timed steps")
 
@@ -399,6 +448,11 @@ def measure(args, workload, sfm, dev, rank, world, sampler, nsets):
     })
     if traffic:
         roof["traffic_over_algorithmic"] = traffic / bytes_launch
+    if roof["bound"] == "hbm":
+        # the stricter of the two denominators is the measured copy rate; the
+        # nominal HBM3e rate, for reference
+        roof["frac_of_nominal"] = achieved_gbs / NOMINAL_HBM_GBS
+        roof["nominal_peak"] = NOMINAL_HBM_GBS
     p0 = sets[0]
     config = {
         "workload": workload, "batch": p0.batch_size, "q_n": p0.num_heads_q, "d": 512,
@@ -413,9 +467,14 @@ def measure(args, workload, sfm, dev, rank, world, sampler, nsets):
         "parallelism": f"replicas x{world}",
         "split_policy": args.split_policy, "work_units": units,
     }
+    fwd_launches = launches_per_step - 1
     res = {
         "workload": workload, "K": K, "W": W, "ms_max": ms_max, "rows_total": rows_total,
         "flops_total": flops_total, "fwd_ms": fwd_ms, "roofline": roof, "config": config,
+        "graph_fwd_ms": graph_ms, "l2_warm_fwd_ms": warm_ms, "planner_ms": plan_ms,
+        "rows_per_step": rows_total / K,
+        # every launch of every timed leg: steps, forwards, graph replays, L2-warm forwards, planner calls
+        "timed_launches": launches_per_step * K + fwd_launches * K + fwd_launches * KG * reps + fwd_launches * K + K,
         "launches_per_step": launches_per_step, "clocks": sampler.summary(t_in, t_out),
         "dtype": {"int8_packed": "fp16 (int8 KV dequantized)", "fp8_packed": "fp16 (fp8 e4m3 KV dequantized)"}
                  .get(p0.kv_format, "bf16"),
@@ -468,7 +527,7 @@ def run_ours(args):
                         "ms_per_step": r["ms_max"] / r["K"], "kernel_ms": r["roofline"]["kernel_ms_avg"],
                         "forward_only_ms_per_step": r["fwd_ms"] / r["K"], "work_units": r["config"]["work_units"],
                         "value": r["rows_total"] / (r["ms_max"] * 1e-3), "steps": r["K"],
-                        "launches": r["launches_per_step"] * r["K"], "clocks_sm_mhz": r["clocks"].get("sm_mhz"),
+                        "launches": r["timed_launches"], "clocks_sm_mhz": r["clocks"].get("sm_mhz"),
                     }
         torch.cuda.empty_cache()
     sampler.stop()
@@ -504,11 +563,23 @@ def run_ours(args):
                              "ms_per_step": fwd_ms / K,
                              "note": "sfm_forward alone (attention and, when rows have several splits, the "
                                      "combine) on plans made beforehand, "
-                                     "as a model reuses one plan across its layers"},
-            "gpu_launches": head["launches_per_step"] * K + (second["launches_per_step"] * second["K"]
-                                                             if second else 0)
+                                     "as a model reuses one plan across its layers",
+                             "cuda_graph": {"value": head["rows_per_step"] / (head["graph_fwd_ms"] * 1e-3),
+                                            "unit": "tokens/s", "ms_per_forward": head["graph_fwd_ms"],
+                                            "note": "the same forwards captured as one CUDA graph of back-to-back "
+                                                    "calls over the rotating sets, replayed"},
+                             "l2_warm": {"value": head["rows_per_step"] / (head["l2_warm_fwd_ms"] * 1e-3),
+                                         "unit": "tokens/s", "ms_per_forward": head["l2_warm_fwd_ms"],
+                                         "note": "L2-warm: one input set's forward repeated, its KV rows left in "
+                                                 "L2 (not the headline)"}},
+            "planner_only": {"ms_per_call": head["planner_ms"],
+                             "note": "sfm_metadata (the device planner) alone, back to back over the sets"},
+            "gpu_launches": head["timed_launches"] + (second["timed_launches"] if second else 0)
                             + (sum(v["launches"] for w in small.values() for b in w.values() for v in b.values())
                                if small else 0),
+            "gpu_launches_note": "launches of this library's kernels in every timed leg of this line (steps, "
+                                 "forward-only, graph replays, L2-warm forwards, planner calls; HCA and small-batch "
+                                 "blocks included)",
             "clocks": head["clocks"],
         }
         if second:
@@ -517,6 +588,8 @@ def run_ours(args):
                 "ms_per_step": second["ms_max"] / second["K"], "steps": second["K"],
                 "tflops": second["flops_total"] / (second["ms_max"] * 1e-3) / 1e12,
                 "forward_only_ms_per_step": second["fwd_ms"] / second["K"],
+                "graph_ms_per_forward": second["graph_fwd_ms"], "l2_warm_ms_per_forward": second["l2_warm_fwd_ms"],
+                "planner_ms_per_call": second["planner_ms"],
                 "roofline": second["roofline"], "config": second["config"], "clocks": second["clocks"],
                 "note": "the second configuration of the >= 70 % roofline target, timed in the same run "
                         "after the headline (its launches are counted in gpu_launches)",
