@@ -241,6 +241,9 @@ OCCUPANCY = {
     "hca_decode_b8": lambda: S.hca_decode(device="cuda", batch=8, compact_pool=True),
     "packed_decode_b3": lambda: S.packed_decode(device="cuda", batch=3, kv_len=8192),
     "packed_fp8_decode_b2": lambda: S.packed_fp8_decode(device="cuda", batch=2, kv_len=8192),
+    # prefill-shaped (more than 16 query rows per sequence: one split per row
+    # by default): 2 sequences of 17-24 rows
+    "csa_prefill_tiny": lambda: S.csa_prefill(device="cuda", nseq=2, qmin=17, qmax=24, prefix_max=3000),
 }
 
 
