@@ -223,12 +223,19 @@ int sfm_workspace_size(const sfm_params *params, size_t *bytes);
 /* "sparse_flash_mla_metadata": enqueue the device-side planner.  It reads the
  * length tensors of `lengths` (cu_seqlens_*, seqused_*, cmp_residual_kv; other
  * fields are ignored and may be NULL), computes every query row's attended-row
- * count, cuts it into equal splits of at most a fixed size (a function of
- * that row's own count and the params only, so a row's result does not depend
- * on the rest of the batch: 确定性计算 / batch invariance) and balances the
- * splits over the SMs.
+ * count, cuts it into equal splits of at most a fixed size (by default a
+ * function of that row's own count and the params only, so a row's result
+ * does not depend on the rest of the batch: 确定性计算 / batch invariance;
+ * see sfm_params.split_policy) and balances the splits over the SMs.
  * metadata: device int32[metadata_n], 16-byte aligned (SFM_ERR_LAYOUT
- * otherwise), metadata_n >= sfm_metadata_size(). */
+ * otherwise), metadata_n >= sfm_metadata_size().
+ * Ordering: the planner is launched as a programmatic dependent of the kernel
+ * before it in the stream and reads the length tensors before waiting for
+ * that kernel to finish (it waits before writing `metadata`).  The kernels
+ * of this library never write length tensors, copies and ordinary kernels
+ * finish before it starts; a kernel of the caller's that triggers its
+ * dependents early (griddepcontrol.launch_dependents) must not write the
+ * length tensors after that trigger. */
 int sfm_metadata(const sfm_params *params, const sfm_tensors *lengths, int32_t *metadata, size_t metadata_n,
                  sfm_stream_t stream);
 

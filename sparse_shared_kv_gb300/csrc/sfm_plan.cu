@@ -95,13 +95,17 @@ __global__ void __launch_bounds__(kPlanThreads) sfm_plan_kernel(KParams kp)
     __shared__ int32_t s_owner[kMaxSplits];       // split -> row (flat record writes)
     __shared__ int64_t s_tot[2];                  // splits, modelled cost
     __shared__ int s_overflow;
+    __shared__ int s_lenflags;                    // length problems, while the rows stay in shared memory
 
     // the attention kernel may start its set-up now; it waits for this grid
     // to finish before it reads the plan.  This grid itself is launched as a
     // dependent of whatever ran before it on the stream (its launch latency
-    // overlaps that kernel's tail) and waits for it before reading any input.
+    // overlaps that kernel's tail).  It reads only the length tensors, which
+    // no kernel of this library writes, and waits for its predecessor before
+    // it writes the plan (a previous forward may still be reading an earlier
+    // plan in the same buffer): while the rows fit in shared memory, the row
+    // phase (the length loads) runs before that wait.
     grid_launch_dependents();
-    grid_dependency_wait();
 
     int32_t *meta = kp.meta_w;
     const int T = kp.T, G = kp.G, S = kp.split_rows;
@@ -113,13 +117,15 @@ __global__ void __launch_bounds__(kPlanThreads) sfm_plan_kernel(KParams kp)
     int32_t *wrec = meta + meta_wrec_off(G, T, kp.wcap);
     const bool in_smem = T <= kSmemRows;
     const int tid = threadIdx.x;
+    if (!in_smem) grid_dependency_wait();
     if (tid == 0) {
         s_overflow = G > kMaxWorkers ? 1 : 0;
         s_tot[0] = s_tot[1] = 0;
-        meta[H_LENFLAGS] = 0;       // length problems found while planning are OR-ed here
+        s_lenflags = 0;
+        if (!in_smem) meta[H_LENFLAGS] = 0;       // length problems found while planning are OR-ed here
     }
     __syncthreads();
-    kp.status = meta + H_LENFLAGS;
+    kp.status = in_smem ? &s_lenflags : meta + H_LENFLAGS;
 
     auto rec_of = [&](int t, int4 &r0, int4 &r1) {
         if (in_smem) {
@@ -165,7 +171,12 @@ __global__ void __launch_bounds__(kPlanThreads) sfm_plan_kernel(KParams kp)
             r[4] = r1.x; r[5] = r1.y; r[6] = r1.z; r[7] = r1.w;
         }
     }
+    if (in_smem) grid_dependency_wait();
     __syncthreads();
+    if (in_smem) {
+        if (tid == 0) meta[H_LENFLAGS] = s_lenflags;
+        kp.status = meta + H_LENFLAGS;
+    }
 
     // 2. split and unit-cost prefixes over contiguous runs of rows per thread
     const int per = (T + kPlanThreads - 1) / kPlanThreads;
@@ -365,8 +376,9 @@ __global__ void __launch_bounds__(kSmallThreads) sfm_plan_small_kernel(KParams k
     __shared__ int s_flags[2];                             // length problems, per row warp
     __shared__ int s_over[2];                              // a row with too many splits, per row warp
 
+    // reads only the length tensors before its dependency wait (the row
+    // phase touches shared memory only); waits before it writes the plan
     grid_launch_dependents();
-    grid_dependency_wait();
 
     int32_t *meta = kp.meta_w;
     const int T = kp.T, G = kp.G;
@@ -413,6 +425,7 @@ __global__ void __launch_bounds__(kSmallThreads) sfm_plan_small_kernel(KParams k
             s_wt[warp][1] = ic;
         }
     }
+    grid_dependency_wait();
     __syncthreads();
 
     // row prefixes over the whole batch (rows past T carry no splits and no cost)
