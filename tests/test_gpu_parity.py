@@ -291,6 +291,27 @@ def test_occupancy_policy_keeps_full_batches_invariant():
     assert torch.equal(oa, ob) and torch.equal(la, lb)
 
 
+def test_plan_sees_lengths_written_just_before():
+    """sfm_metadata reads the length tensors before it waits for the kernel
+    before it in the stream; a kernel that does not release its dependents
+    early (torch's, like most) still orders its writes first: lengths
+    shortened by a torch kernel right before the plan, on the same stream
+    with no synchronisation, are the ones the plan and the forward use."""
+    prob = S.csa_decode(device="cuda", batch=4, seed=17)
+    r = _sfm.Runner(prob)
+    _, _, status = r.run()
+    assert status == 0
+    torch.cuda.synchronize()
+    prob.t["seqused_ori_kv"].sub_(3)        # the window moves back three rows
+    r.status.zero_()
+    r.plan()
+    r.forward()
+    torch.cuda.synchronize()
+    assert int(r.status.item()) == 0
+    host = prob.to("cpu")
+    assert_parity(prob, r.out, r.lse, host=host)
+
+
 def test_context_parallel_split_on_gpu():
     from tests.test_oracle_pins import _cp_slice
     g = S.build("cp_global", seed=21, q_n=64, q_lens=[16, 18], kv_lens=[16, 18], cmp_lens=[4, 4],
