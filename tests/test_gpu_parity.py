@@ -164,6 +164,24 @@ def test_csa_topk_1024(batch):
     assert_sets(prob, tokens=tokens, host=host, out=out, lse=lse)
 
 
+@pytest.mark.parametrize("mode", ["csa", "hca"])
+def test_largest_pages(mode):
+    """Paged ori and cmp caches with the largest page the parameter rules
+    allow (1024 rows per block): windows and compressed rows that straddle
+    page boundaries, every row against the oracle, attended sets exact."""
+    kw = dict(q_n=64, q_lens=[1, 1, 1], kv_lens=[5000, 2100, 9000], layout_q="BSND", layout_kv="PAGED",
+              mode=mode, cmp_ratio=4 if mode == "csa" else 16, ori_block_size=1024, cmp_block_size=1024,
+              sinks=True)
+    if mode == "csa":
+        kw["cmp_topk"] = 512
+    prob = S.build(f"pages1024_{mode}", seed=23, device="cuda", **kw)
+    out, lse, status = _sfm.run(prob)
+    assert status == 0, hex(status)
+    host = prob.to("cpu")
+    assert_parity(prob, out, lse, host=host)
+    assert_sets(prob, host=host, out=out, lse=lse)
+
+
 def test_fp16_and_lse_off():
     prob = S.build("fp16_nolse", seed=5, device="cuda", q_n=64, q_lens=[1, 1], kv_lens=[900, 4000],
                    layout_q="BSND", layout_kv="PAGED", mode="hca", cmp_ratio=16, dtype="fp16", sinks=True,
