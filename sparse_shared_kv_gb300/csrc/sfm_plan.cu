@@ -365,6 +365,8 @@ __global__ void __launch_bounds__(kPlanThreads) sfm_plan_kernel(KParams kp)
 // No thread runs a serial walk; the general kernel above serves larger batches.
 constexpr int kSmallRows = 64;
 constexpr int kSmallThreads = 512;
+constexpr int kStageSplits = 384;        // plans this small are finished in shared memory
+constexpr int kStageWorkers = 256;       // before the dependency wait, then streamed out
 
 __global__ void __launch_bounds__(kSmallThreads) sfm_plan_small_kernel(KParams kp)
 {
@@ -375,6 +377,8 @@ __global__ void __launch_bounds__(kSmallThreads) sfm_plan_small_kernel(KParams k
     __shared__ int32_t s_ws[kSmallThreads], s_wrow[kSmallThreads];
     __shared__ int s_flags[2];                             // length problems, per row warp
     __shared__ int s_over[2];                              // a row with too many splits, per row warp
+    __shared__ int4 s_srec[kStageSplits * 3];              // staged split records (words 0..11)
+    __shared__ int4 s_wrec[kStageWorkers * 4];             // staged worker records
 
     // reads only the length tensors before its dependency wait (the row
     // phase touches shared memory only); waits before it writes the plan
@@ -425,7 +429,6 @@ __global__ void __launch_bounds__(kSmallThreads) sfm_plan_small_kernel(KParams k
             s_wt[warp][1] = ic;
         }
     }
-    grid_dependency_wait();
     __syncthreads();
 
     // row prefixes over the whole batch (rows past T carry no splits and no cost)
@@ -449,28 +452,19 @@ __global__ void __launch_bounds__(kSmallThreads) sfm_plan_small_kernel(KParams k
         const int2 sh = s_shape[t];
         return make_int4(t, (int32_t)(incl_s(t) - sh.x), sh.x, sh.y);
     };
-
-    // 2. the split table, the split records (flat), and each worker's first unit
-    if (tid <= T) sp[tid] = tid < T ? (int32_t)(incl_s(tid) - s_shape[tid].x) : (int32_t)(W < INT32_MAX ? W : INT32_MAX);
     const int64_t WR = (W < kp.wcap ? W : kp.wcap) * 3;
-    if (WR <= INT32_MAX) {                   // 32-bit index arithmetic
-        for (int i = tid; i < (int)WR; i += kSmallThreads) {
-            const int w = i / 3, part = i - w * 3;
-            reinterpret_cast<int4 *>(srec + (int64_t)w * kSrecWords)[part] = row_word(find_row(w, false), part);
-        }
-    } else {
-        for (int64_t i = tid; i < WR; i += kSmallThreads) {
-            const int64_t w = i / 3;
-            const int part = (int)(i - w * 3);
-            reinterpret_cast<int4 *>(srec + w * kSrecWords)[part] = row_word(find_row(w, false), part);
-        }
-    }
+    // a small plan is finished in shared memory before the dependency wait
+    // (only its stores wait for the previous kernel); larger ones are
+    // computed and written after it
+    const bool staged = WR <= kStageSplits * 3 && G <= kStageWorkers;
+
+    // 2. each worker's first unit (the row whose cost span holds c total / G,
+    // then the unit inside it by one division), and the split records
     if (tid <= G) {
         int32_t u = 0, row = 0;
         if (tid == G) {
             u = (int32_t)(units < INT32_MAX ? units : INT32_MAX);
         } else if (total > 0) {
-            // target(c) = floor(c total / G): the unit whose modelled-cost span holds it
             const int64_t num = (int64_t)tid * total;
             const int64_t tgt = (total + 1) * (G + 1) <= 0xffffffffll ? (int64_t)udiv_est((uint32_t)num, (uint32_t)G)
                                                                      : num / G;
@@ -484,19 +478,59 @@ __global__ void __launch_bounds__(kSmallThreads) sfm_plan_small_kernel(KParams k
         }
         s_ws[tid] = u;
         s_wrow[tid] = row;
-        meta[meta_ws_off() + tid] = u;
     }
-    __syncthreads();
+    if (staged) {
+        for (int i = tid; i < (int)WR; i += kSmallThreads) {
+            const int w = i / 3, part = i - w * 3;
+            s_srec[i] = row_word(find_row(w, false), part);
+        }
+        __syncthreads();
+        // 3. worker records: the unit range, then the first unit's split record words
+        for (int i = tid; i < G * 4; i += kSmallThreads) {
+            const int c = i >> 2, part = i & 3;
+            const int32_t u0 = s_ws[c], u1 = s_ws[c + 1];
+            s_wrec[i] = part == 0 ? make_int4(u0, u1, 0, 0)
+                                  : (u0 < u1 ? row_word(s_wrow[c], part - 1) : make_int4(0, 0, 0, 0));
+        }
+        __syncthreads();
+    }
 
-    // 3. worker records: the unit range, then the first unit's split record words
-    for (int i = tid; i < G * 4; i += kSmallThreads) {
-        const int c = i >> 2, part = i & 3;
-        const int32_t u0 = s_ws[c], u1 = s_ws[c + 1];
-        int4 v;
-        if (part == 0) v = make_int4(u0, u1, 0, 0);
-        else if (u0 < u1) v = row_word(s_wrow[c], part - 1);
-        else continue;              // an empty range: the rest of the record is never read
-        reinterpret_cast<int4 *>(wrec + (int64_t)c * kWrecWords)[part] = v;
+    grid_dependency_wait();                  // the plan may now be overwritten
+
+    if (tid <= T) sp[tid] = tid < T ? (int32_t)(incl_s(tid) - s_shape[tid].x) : (int32_t)(W < INT32_MAX ? W : INT32_MAX);
+    if (tid <= G) meta[meta_ws_off() + tid] = s_ws[tid];
+    if (staged) {
+        for (int i = tid; i < (int)WR; i += kSmallThreads)
+            reinterpret_cast<int4 *>(srec + (int64_t)(i / 3) * kSrecWords)[i % 3] = s_srec[i];
+        for (int i = tid; i < G * 4; i += kSmallThreads) {
+            const int c = i >> 2, part = i & 3;
+            if (part == 0 || s_ws[c] < s_ws[c + 1])          // an empty range: the rest is never read
+                reinterpret_cast<int4 *>(wrec + (int64_t)c * kWrecWords)[part] = s_wrec[i];
+        }
+    } else {
+        if (WR <= INT32_MAX) {                   // 32-bit index arithmetic
+            for (int i = tid; i < (int)WR; i += kSmallThreads) {
+                const int w = i / 3, part = i - w * 3;
+                reinterpret_cast<int4 *>(srec + (int64_t)w * kSrecWords)[part] = row_word(find_row(w, false), part);
+            }
+        } else {
+            for (int64_t i = tid; i < WR; i += kSmallThreads) {
+                const int64_t w = i / 3;
+                const int part = (int)(i - w * 3);
+                reinterpret_cast<int4 *>(srec + w * kSrecWords)[part] = row_word(find_row(w, false), part);
+            }
+        }
+        __syncthreads();
+        // 3. worker records: the unit range, then the first unit's split record words
+        for (int i = tid; i < G * 4; i += kSmallThreads) {
+            const int c = i >> 2, part = i & 3;
+            const int32_t u0 = s_ws[c], u1 = s_ws[c + 1];
+            int4 v;
+            if (part == 0) v = make_int4(u0, u1, 0, 0);
+            else if (u0 < u1) v = row_word(s_wrow[c], part - 1);
+            else continue;              // an empty range: the rest of the record is never read
+            reinterpret_cast<int4 *>(wrec + (int64_t)c * kWrecWords)[part] = v;
+        }
     }
     if (tid == 0) {
         const bool bad = W > INT32_MAX || units > INT32_MAX || W > kp.wcap || total > INT32_MAX;
