@@ -427,7 +427,8 @@ def test_packed_128_heads_row_without_positions(fmt, return_lse):
     assert_sets(prob, out=out, lse=lse)
 
 
-def test_public_two_call_api():
+@pytest.mark.parametrize("batch_invariant", [True, False], ids=["invariant", "occupancy"])
+def test_public_two_call_api(batch_invariant):
     prob = S.csa_decode(device="cuda", batch=3)
     T = prob.t
     md = sfm.sparse_flash_mla_metadata(
@@ -435,7 +436,8 @@ def test_public_two_call_api():
         cmp_residual_kv=T["cmp_residual_kv"], batch_size=3, max_seqlen_q=1, max_seqlen_ori_kv=prob.max_seqlen_ori_kv,
         max_seqlen_cmp_kv=prob.max_seqlen_cmp_kv, cmp_topk=512, cmp_ratio=4, ori_mask_mode=4, cmp_mask_mode=3,
         ori_win_left=127, ori_win_right=0, layout_q="BSND", layout_kv="PAGED", ori_block_size=128,
-        cmp_block_size=128, return_softmax_lse=True)
+        cmp_block_size=128, return_softmax_lse=True, batch_invariant=batch_invariant)
+    assert md.params.split_policy == (sfm.SPLIT_BATCH_INVARIANT if batch_invariant else sfm.SPLIT_OCCUPANCY)
     out, lse = sfm.sparse_flash_mla(
         T["q"], metadata=md, ori_kv=T["ori_kv"], cmp_kv=T["cmp_kv"], cmp_sparse_indices=T["cmp_sparse_indices"],
         ori_block_table=T["ori_block_table"], cmp_block_table=T["cmp_block_table"],
