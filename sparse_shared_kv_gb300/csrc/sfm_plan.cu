@@ -353,7 +353,7 @@ __global__ void __launch_bounds__(kPlanThreads) sfm_plan_kernel(KParams kp)
 }
 
 // The same plan for a decode batch of at most kSmallRows rows and fewer than
-// kSmallThreads workers, in three short phases and two block barriers:
+// kSmallThreads workers, in three short phases:
 //   1. warps 0 and 1 take one row per lane (lengths, window, counts, split
 //      shape) and scan the split counts and modelled costs of their 32 rows
 //      with shuffles;
@@ -361,8 +361,13 @@ __global__ void __launch_bounds__(kPlanThreads) sfm_plan_kernel(KParams kp)
 //      of each split record it writes (one flat stream) and the first unit of
 //      worker c = thread index (the row whose cost span holds c total / G,
 //      then the unit inside it by one division);
-//   3. the worker records go out as one flat stream.
-// No thread runs a serial walk; the general kernel above serves larger batches.
+//   3. the worker records, as one flat stream.
+// A plan of at most kStageSplits splits and kStageWorkers workers is built
+// entirely in shared memory before the kernel's dependency wait (it reads
+// only the length tensors) and only streamed out after it, so its
+// computation overlaps the previous kernel; larger plans are built and
+// written after the wait.  No thread runs a serial walk; the general kernel
+// above serves larger batches.
 constexpr int kSmallRows = 64;
 constexpr int kSmallThreads = 512;
 constexpr int kStageSplits = 384;        // plans this small are finished in shared memory
@@ -380,8 +385,8 @@ __global__ void __launch_bounds__(kSmallThreads) sfm_plan_small_kernel(KParams k
     __shared__ int4 s_srec[kStageSplits * 3];              // staged split records (words 0..11)
     __shared__ int4 s_wrec[kStageWorkers * 4];             // staged worker records
 
-    // reads only the length tensors before its dependency wait (the row
-    // phase touches shared memory only); waits before it writes the plan
+    // reads only the length tensors before its dependency wait (everything
+    // up to the stores works in shared memory); waits before it writes the plan
     grid_launch_dependents();
 
     int32_t *meta = kp.meta_w;
