@@ -64,6 +64,8 @@ def parse():
                     help="sfm_params.split_policy: batch-invariant splits (the default) or occupancy splits")
     ap.add_argument("--no-small-batch", action="store_true",
                     help="skip the small-batch block (CSA / HCA decode at B = 4, 8, 16 under both split policies)")
+    ap.add_argument("--streams", type=int, default=8,
+                    help="streams that the concurrent-step and end-to-end legs spread independent input sets over")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     return ap.parse_args()
 
@@ -146,7 +148,7 @@ class ClockSampler:
             except subprocess.TimeoutExpired:
                 self.proc.kill()
 
-    def summary(self, t0=None, t1=None):
+    def summary(self, t0=None, t1=None, t1_legs=None):
         rows = []
         for ts, line in self.lines:
             parts = [p.strip() for p in line.split(",")]
@@ -160,6 +162,12 @@ class ClockSampler:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"], "samples": 0}
         inside = [r for r in rows if (t0 is None or r[0] >= t0) and (t1 is None or r[0] <= t1)]
         window = "timed region"
+        if len(inside) < 5 and t1_legs is not None:
+            # a timed region of a few ms holds few 200 ms samples: take every
+            # timed leg of the workload (they follow the steps back to back)
+            legs = [r for r in rows if (t0 is None or r[0] >= t0) and r[0] <= t1_legs]
+            if len(legs) > len(inside):
+                inside, window = legs, "timed steps and the timed legs after them"
         if not inside:
             inside, window = rows, "warm-up + timed region"
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
@@ -414,6 +422,46 @@ def measure(args, workload, sfm, dev, rank, world, sampler, nsets):
     m1.record(stream)
     torch.cuda.synchronize()
     plan_ms = max_over_ranks(m0.elapsed_time(m1), world, dev) / K
+
+    # independent steps (different input sets: their own plans, workspaces and
+    # outputs) dealt round robin over several streams: the kernels of
+    # different steps run concurrently and fill each other's latency gaps, as
+    # independent batches served side by side would; a set's next step waits
+    # for its previous one (an event), whichever stream that ran on
+    ns = max(1, min(args.streams, len(runners)))
+    cstreams = [torch.cuda.Stream(device=dev) for _ in range(ns)]
+    done = [None] * len(runners)
+
+    def cstep(k):
+        i = k % len(runners)
+        p, params, tens, md, ws, out, lse = runners[i]
+        cs = cstreams[k % ns]
+        if done[i] is not None:
+            cs.wait_event(done[i])
+        sfm.sfm_metadata(params, tens, md, cs)
+        sfm.sfm_forward(params, tens, md, p.softmax_scale, out, lse, ws, status, cs)
+        done[i] = torch.cuda.Event()
+        done[i].record(cs)
+
+    for s_ in cstreams:
+        s_.wait_stream(stream)
+    for k in range(W):
+        cstep(k)
+    for s_ in cstreams:
+        stream.wait_stream(s_)
+    torch.cuda.synchronize()
+    c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    c0.record(stream)
+    for s_ in cstreams:
+        s_.wait_stream(stream)
+    for k in range(K):
+        cstep(k)
+    for s_ in cstreams:
+        stream.wait_stream(s_)
+    c1.record(stream)
+    torch.cuda.synchronize()
+    t_legs = sampler.mark()
+    conc_ms = max_over_ranks(c0.elapsed_time(c1), world, dev)
     if int(status.item()) != 0:
         raise RuntimeError(f"{workload}: device status {int(status.item()):#x} during the timed steps")
 
@@ -473,10 +521,13 @@ def measure(args, workload, sfm, dev, rank, world, sampler, nsets):
         "workload": workload, "K": K, "W": W, "ms_max": ms_max, "rows_total": rows_total,
         "flops_total": flops_total, "fwd_ms": fwd_ms, "roofline": roof, "config": config,
         "graph_fwd_ms": graph_ms, "l2_warm_fwd_ms": warm_ms, "planner_ms": plan_ms,
+        "concurrent_ms": conc_ms, "concurrent_streams": ns,
         "rows_per_step": rows_total / K,
-        # every launch of every timed leg: steps, forwards, graph replays, L2-warm forwards, planner calls
-        "timed_launches": launches_per_step * K + fwd_launches * K + fwd_launches * KG * reps + fwd_launches * K + K,
-        "launches_per_step": launches_per_step, "clocks": sampler.summary(t_in, t_out),
+        # every launch of every timed leg: steps, forwards, graph replays, L2-warm forwards, planner calls,
+        # concurrent steps
+        "timed_launches": launches_per_step * K + fwd_launches * K + fwd_launches * KG * reps + fwd_launches * K + K
+                          + launches_per_step * K,
+        "launches_per_step": launches_per_step, "clocks": sampler.summary(t_in, t_out, t_legs),
         "dtype": {"int8_packed": "fp16 (int8 KV dequantized)", "fp8_packed": "fp16 (fp8 e4m3 KV dequantized)"}
                  .get(p0.kv_format, "bf16"),
     }
@@ -575,12 +626,18 @@ def run_ours(args):
                                                  "L2 (not the headline)"}},
             "planner_only": {"ms_per_call": head["planner_ms"],
                              "note": "sfm_metadata (the device planner) alone, back to back over the sets"},
+            "concurrent_steps": {"value": head["rows_total"] / (head["concurrent_ms"] * 1e-3), "unit": "tokens/s",
+                                 "ms_per_step": head["concurrent_ms"] / K, "streams": head["concurrent_streams"],
+                                 "note": "the same steps (planner + forward, inputs resident) with consecutive "
+                                         "independent input sets spread over several streams, so kernels of "
+                                         "different steps run concurrently; the headline value runs them back to "
+                                         "back on one stream"},
             "gpu_launches": head["timed_launches"] + (second["timed_launches"] if second else 0)
                             + (sum(v["launches"] for w in small.values() for b in w.values() for v in b.values())
                                if small else 0),
             "gpu_launches_note": "launches of this library's kernels in every timed leg of this line (steps, "
-                                 "forward-only, graph replays, L2-warm forwards, planner calls; HCA and small-batch "
-                                 "blocks included)",
+                                 "forward-only, graph replays, L2-warm forwards, planner calls, concurrent steps; "
+                                 "HCA and small-batch blocks included)",
             "clocks": head["clocks"],
         }
         if second:
@@ -591,6 +648,8 @@ def run_ours(args):
                 "forward_only_ms_per_step": second["fwd_ms"] / second["K"],
                 "graph_ms_per_forward": second["graph_fwd_ms"], "l2_warm_ms_per_forward": second["l2_warm_fwd_ms"],
                 "planner_ms_per_call": second["planner_ms"],
+                "concurrent_ms_per_step": second["concurrent_ms"] / second["K"],
+                "concurrent_streams": second["concurrent_streams"],
                 "roofline": second["roofline"], "config": second["config"], "clocks": second["clocks"],
                 "note": "the second configuration of the >= 70 % roofline target, timed in the same run "
                         "after the headline (its launches are counted in gpu_launches)",
@@ -614,8 +673,9 @@ def run_e2e(args, sfm, sets, acc, dev, stream):
     inputs (all of them packed in one pinned buffer), sparse_flash_mla_metadata,
     sparse_flash_mla, one device->host copy of O and LSE.  Each input set's step
     is captured once as a CUDA graph of exactly those calls (as a decode loop
-    would), and consecutive steps (independent batches) are replayed on two
-    streams, so one step's copies overlap another step's kernels."""
+    would), and consecutive steps (independent batches) are replayed on several
+    streams (--streams), so one step's copies overlap other steps' kernels and
+    kernels of different steps run concurrently."""
     names = ("q", "cmp_sparse_indices", "ori_sparse_indices", "ori_block_table", "cmp_block_table",
              "seqused_ori_kv", "seqused_cmp_kv", "cmp_residual_kv", "sinks")
 
@@ -684,12 +744,21 @@ def run_e2e(args, sfm, sets, acc, dev, stream):
         legs.append(g)
         keep.append((hbuf, dbuf, obuf, ohost, T, out, lse))
     torch.cuda.synchronize()
-    streams = [torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)]
+    ns = max(1, min(args.streams, len(legs)))
+    streams = [torch.cuda.Stream(device=dev) for _ in range(ns)]
+    done = [None] * len(legs)
 
     def step(k):
+        # steps dealt round robin over the streams; a set's graph replays only
+        # after its previous replay (its buffers are reused), on whichever stream
         i = k % len(legs)
-        with torch.cuda.stream(streams[i % 2]):     # a set's graph always replays on the same stream
+        st = streams[k % ns]
+        if done[i] is not None:
+            st.wait_event(done[i])
+        with torch.cuda.stream(st):
             legs[i].replay()
+        done[i] = torch.cuda.Event()
+        done[i].record(st)
 
     for k in range(max(3, 2 * len(legs))):
         step(k)
@@ -710,7 +779,7 @@ def run_e2e(args, sfm, sets, acc, dev, stream):
     return {"ms_total": e0.elapsed_time(e1), "steps": K, "rows": rows, "h2d": h2d, "d2h": d2h,
             "mode": "per step: one H2D copy of all inputs from pinned memory, the public two-call API, one D2H "
                     "copy of O and LSE; each input set's step captured once as a CUDA graph, consecutive "
-                    "(independent) steps replayed on two streams"}
+                    "(independent) steps replayed on %d streams" % ns}
 
 
 # ---------------------------------------------------------------------------
