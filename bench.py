@@ -110,18 +110,71 @@ def sum_over_ranks(x: float, world: int, device) -> float:
 # ---------------------------------------------------------------------------
 # clocks during the timed region
 # ---------------------------------------------------------------------------
+class _NvmlClocks:
+    """SM clock and clock-event reasons read through the driver's NVML
+    library (read-only queries, microseconds each), for sampling far more
+    often than nvidia-smi's loop delivers lines."""
+    CLOCK_SM = 1                       # NVML_CLOCK_SM
+    # clock-event reason bits of NVML's public header
+    BITS = ((0x8, "hw_slowdown"), (0x40, "hw_thermal_slowdown"), (0x20, "sw_thermal_slowdown"),
+            (0x4, "sw_power_cap"))
+
+    def __init__(self, uuid: str):
+        import ctypes
+        self.ct = ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit_v2 failed")
+        self.lib = lib
+        self.h = ctypes.c_void_p()
+        if lib.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(self.h)) != 0:
+            raise OSError("no NVML handle for " + uuid)
+        try:
+            self.reasons_fn = lib.nvmlDeviceGetCurrentClocksEventReasons
+        except AttributeError:
+            self.reasons_fn = lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        mx = ctypes.c_uint()
+        if lib.nvmlDeviceGetMaxClockInfo(self.h, self.CLOCK_SM, ctypes.byref(mx)) != 0:
+            raise OSError("nvmlDeviceGetMaxClockInfo failed")
+        self.max_mhz = float(mx.value)
+
+    def read(self):
+        sm, bits = self.ct.c_uint(), self.ct.c_ulonglong()
+        if self.lib.nvmlDeviceGetClockInfo(self.h, self.CLOCK_SM, self.ct.byref(sm)) != 0:
+            return None
+        if self.reasons_fn(self.h, self.ct.byref(bits)) != 0:
+            return None
+        return float(sm.value), [n for b, n in self.BITS if bits.value & b]
+
+
 class ClockSampler:
+    """Clocks and throttle reasons while the bench runs: nvidia-smi's query
+    loop and, where the driver's NVML library loads, a 2 ms NVML poll (the
+    timed steps of a decode workload last milliseconds, shorter than
+    nvidia-smi's line interval on these hosts)."""
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
 
     def __init__(self, gpu_id: str):
         self.gpu_id = gpu_id
         self.proc = None
         self.lines = []
         self.t = None
+        self.nvml = None
+        self.nv_rows = []
+        self.done = threading.Event()
+        self.poller = None
 
     def start(self):
+        try:
+            self.nvml = _NvmlClocks(self.gpu_id)
+        except (OSError, AttributeError):
+            self.nvml = None
+        if self.nvml is not None:
+            self.poller = threading.Thread(target=self._poll, daemon=True)
+            self.poller.start()
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", self.gpu_id, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
@@ -137,10 +190,18 @@ class ClockSampler:
         for line in self.proc.stdout:
             self.lines.append((time.time(), line.strip()))
 
+    def _poll(self):
+        while not self.done.is_set():
+            v = self.nvml.read()
+            if v is not None:
+                self.nv_rows.append((time.time(), v[0], self.nvml.max_mhz, v[1]))
+            time.sleep(0.002)
+
     def mark(self):
         return time.time()
 
     def stop(self):
+        self.done.set()
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -148,37 +209,43 @@ class ClockSampler:
             except subprocess.TimeoutExpired:
                 self.proc.kill()
 
-    def summary(self, t0=None, t1=None, t1_legs=None):
+    def _smi_rows(self):
         rows = []
         for ts, line in self.lines:
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 8:
                 continue
             try:
-                rows.append((ts, float(parts[0]), float(parts[1]), parts[3:]))
+                active = [n for n, f in zip(self.NAMES, parts[4:8]) if f.lower() == "active"]
+                rows.append((ts, float(parts[0]), float(parts[1]), active))
             except ValueError:
                 continue
+        return rows
+
+    def summary(self, t0=None, t1=None, t1_legs=None, t0_warm=None):
+        rows, source = list(self.nv_rows), "NVML, 2 ms poll"
         if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"], "samples": 0}
+            rows, source = self._smi_rows(), "nvidia-smi"
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no clock samples"], "samples": 0}
         inside = [r for r in rows if (t0 is None or r[0] >= t0) and (t1 is None or r[0] <= t1)]
         window = "timed region"
         if len(inside) < 5 and t1_legs is not None:
-            # a timed region of a few ms holds few 200 ms samples: take every
-            # timed leg of the workload (they follow the steps back to back)
+            # a timed region of a few ms holds few samples: take every timed
+            # leg of the workload (they follow the steps back to back), then
+            # the whole run of the workload from its first warm-up step
             legs = [r for r in rows if (t0 is None or r[0] >= t0) and r[0] <= t1_legs]
             if len(legs) > len(inside):
                 inside, window = legs, "timed steps and the timed legs after them"
+            if len(inside) < 5 and t0_warm is not None:
+                busy = [r for r in rows if t0_warm <= r[0] <= t1_legs]
+                if len(busy) > len(inside):
+                    inside, window = busy, "warm-up, timed steps and the timed legs after them"
         if not inside:
             inside, window = rows, "warm-up + timed region"
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = set()
-        for r in inside:
-            flags = r[3][1:]
-            for n, f in zip(names, flags):
-                if f.strip().lower() == "active":
-                    reasons.add(n)
+        reasons = sorted({n for r in inside for n in r[3]})
         return {"sm_mhz": statistics.median(r[1] for r in inside), "sm_max_mhz": max(r[2] for r in inside),
-                "reasons": sorted(reasons), "samples": len(inside), "window": window}
+                "reasons": reasons, "samples": len(inside), "window": window, "source": source}
 
 
 # ---------------------------------------------------------------------------
@@ -317,6 +384,7 @@ def measure(args, workload, sfm, dev, rank, world, sampler, nsets):
         sfm.sfm_forward(params, tens, md, p.softmax_scale, out, lse, ws, status, stream)
 
     W = max(args.warmup, 3)
+    t_warm = sampler.mark()
     for k in range(W):
         step(k)
     torch.cuda.synchronize()
@@ -527,7 +595,7 @@ def measure(args, workload, sfm, dev, rank, world, sampler, nsets):
         # concurrent steps
         "timed_launches": launches_per_step * K + fwd_launches * K + fwd_launches * KG * reps + fwd_launches * K + K
                           + launches_per_step * K,
-        "launches_per_step": launches_per_step, "clocks": sampler.summary(t_in, t_out, t_legs),
+        "launches_per_step": launches_per_step, "clocks": sampler.summary(t_in, t_out, t_legs, t_warm),
         "dtype": {"int8_packed": "fp16 (int8 KV dequantized)", "fp8_packed": "fp16 (fp8 e4m3 KV dequantized)"}
                  .get(p0.kv_format, "bf16"),
     }
