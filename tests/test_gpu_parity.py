@@ -505,6 +505,50 @@ def test_two_call_api_in_cuda_graphs_on_two_streams():
         assert_parity(prob, o, l)
 
 
+def test_independent_problems_on_eight_streams():
+    """Independent problems (CSA decode, HCA decode, packed INT8 decode, CSA
+    prefill, each with its own plan, workspace and outputs) dealt round robin
+    over eight streams for several rounds, a problem's next step ordered
+    after its previous one by an event, so kernels of different problems run
+    at the same time: every result equals the problem's eager result bit for
+    bit and meets the oracle."""
+    probs = [S.csa_decode(device="cuda", batch=4, seed=81), S.csa_decode(device="cuda", batch=9, seed=82),
+             S.hca_decode(device="cuda", batch=2, compact_pool=True, seed=83),
+             S.packed_decode(device="cuda", batch=2, kv_len=4096, seed=84),
+             S.csa_prefill(device="cuda", nseq=2, qmin=40, qmax=120, prefix_max=500, seed=85),
+             S.csa_decode(device="cuda", batch=3, cmp_topk=1024, seed=86)]
+    runners = [_sfm.Runner(p) for p in probs]
+    eager = []
+    for r in runners:
+        out, lse, status = r.run()
+        assert status == 0, hex(status)
+        eager.append((out.clone(), lse.clone()))
+        r.out.zero_()
+        r.lse.zero_()
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream() for _ in range(8)]
+    done = [None] * len(runners)
+    cur = torch.cuda.current_stream()
+    for st in streams:
+        st.wait_stream(cur)
+    for k in range(4 * len(runners)):
+        i = k % len(runners)
+        st = streams[k % len(streams)]
+        if done[i] is not None:
+            st.wait_event(done[i])
+        runners[i].plan(st)
+        runners[i].forward(st)
+        done[i] = torch.cuda.Event()
+        done[i].record(st)
+    for st in streams:
+        cur.wait_stream(st)
+    torch.cuda.synchronize()
+    for prob, r, (eo, el) in zip(probs, runners, eager):
+        assert int(r.status.item()) == 0
+        assert torch.equal(r.out, eo) and torch.equal(r.lse, el), prob.name
+        assert_parity(prob, r.out, r.lse)
+
+
 # ---------------------------------------------------------------------------
 # the attention kernel's code paths: head counts, split counts, dtypes,
 # block-wise selection, packed formats
