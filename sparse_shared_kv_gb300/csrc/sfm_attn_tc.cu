@@ -935,9 +935,9 @@ __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(const KParams 
                         // only orders the row-mask word
                         if (!warp_wait(bar(B_KV_FULL + st), use & 1, abort_flag)) { stop = true; break; }
                     }
+                    float x[NT];
                     if (live_head) {
                         const uint32_t vm = valid_s[st];
-                        float x[NT];
 #pragma unroll
                         for (int j = 0; j < NT; ++j) x[j] = ((vm >> j) & 1u) ? __uint_as_float(sv[j]) : -INFINITY;
                         float mx[NT / 2];
@@ -952,6 +952,14 @@ __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(const KParams 
                             alpha = (m == -INFINITY) ? 0.f : fast_exp2(m - tmax);
                             m = tmax;
                         }
+                    }
+                    // the tile's rescale factor is final once its maximum is
+                    // known: published before the exponentials, so warps 6-7
+                    // (and the P.V issue behind them) need not wait for those
+                    alpha_s[(gi & 3) * 64 + r] = alpha;      // four-slot ring, whatever the stage count
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(B_ALPHA + (gi & 3)));
+                    if (live_head) {
                         float ps[NT / 2];
                         if (m == -INFINITY) {
 #pragma unroll
@@ -975,9 +983,6 @@ __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(const KParams 
                             for (int j = 0; j < w2; ++j) ps[j] += ps[j + w2];
                         l = l * alpha + ps[0];
                     }
-                    alpha_s[(gi & 3) * 64 + r] = alpha;      // four-slot ring, whatever the stage count
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(bar(B_ALPHA + (gi & 3)));
                 } else {
                     if constexpr (EX) {
                         // V of the tile: once every S product has read the
