@@ -795,10 +795,11 @@ __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(const KParams 
                     if constexpr (!EX) {
                         // this warp's chain c covers reduction steps [kSteps c, kSteps (c + 1)).
                         // Each descriptor is built here, which paces the products at ~50 ns
-                        // instead of ~30: issued back to back they read Q (4 KB per product)
-                        // from shared memory fast enough to slow the copies and the P.V that
-                        // frees a stage (CSA prefill +24 %, HCA decode +3 %, FP8 rows +6 % in
-                        // A/B runs on one GPU).
+                        // instead of ~30.  Issued back to back from precomputed descriptors
+                        // they made every workload slower (CSA prefill +24 %, HCA decode
+                        // +3 %, FP8 rows +6 % in A/B runs on one GPU), and still did as M=64
+                        // products (half of Q's shared-memory reads) or with the S issuers
+                        // yielding to a pending P.V.
                         constexpr int kSteps = QB * 4 / kChains;
 #pragma unroll 3
                         for (int k = 0; k < kSteps; ++k) {
