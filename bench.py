@@ -509,18 +509,21 @@ def measure(args, workload, sfm, dev, rank, world, sampler, nsets):
     # for its previous one (an event), whichever stream that ran on
     ns = max(1, min(args.streams, len(runners)))
     cstreams = [torch.cuda.Stream(device=dev) for _ in range(ns)]
-    done = [None] * len(runners)
+    # one event per set, re-recorded each step (a wait takes the event as it
+    # stands when the wait is enqueued)
+    done = [torch.cuda.Event() for _ in runners]
+    used = [False] * len(runners)
 
     def cstep(k):
         i = k % len(runners)
         p, params, tens, md, ws, out, lse = runners[i]
         cs = cstreams[k % ns]
-        if done[i] is not None:
+        if used[i]:
             cs.wait_event(done[i])
         sfm.sfm_metadata(params, tens, md, cs)
         sfm.sfm_forward(params, tens, md, p.softmax_scale, out, lse, ws, status, cs)
-        done[i] = torch.cuda.Event()
         done[i].record(cs)
+        used[i] = True
 
     for s_ in cstreams:
         s_.wait_stream(stream)
@@ -829,19 +832,20 @@ def run_e2e(args, sfm, sets, acc, dev, stream):
     torch.cuda.synchronize()
     ns = max(1, min(args.streams, len(legs)))
     streams = [torch.cuda.Stream(device=dev) for _ in range(ns)]
-    done = [None] * len(legs)
+    done = [torch.cuda.Event() for _ in legs]       # one per set, re-recorded each step
+    used = [False] * len(legs)
 
     def step(k):
         # steps dealt round robin over the streams; a set's graph replays only
         # after its previous replay (its buffers are reused), on whichever stream
         i = k % len(legs)
         st = streams[k % ns]
-        if done[i] is not None:
+        if used[i]:
             st.wait_event(done[i])
         with torch.cuda.stream(st):
             legs[i].replay()
-        done[i] = torch.cuda.Event()
         done[i].record(st)
+        used[i] = True
 
     for k in range(max(3, 2 * len(legs))):
         step(k)
