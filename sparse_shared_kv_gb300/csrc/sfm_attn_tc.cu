@@ -515,13 +515,21 @@ __global__ void __launch_bounds__(kThreads, 1) sfm_attn_tc_kernel(const KParams 
                     if (i0 + j < s.ntiles && gi >= kStages && (pf_all || gi < kStages + kPrefetchTiles) && ent[j] != -1) {
                         const int64_t r = ent[j] & 0x7fffffff;
                         const uint8_t *row = ent[j] < 0 ? kp.cmp_kv + r * kp.cmp_row_stride : kp.ori_kv + r * kp.ori_row_stride;
-                        constexpr uint32_t kRowBytes = PK ? PK_ROW : QB * 128u;
                         if constexpr (!PK) {
-                            prefetch_l2(row, kRowBytes);         // one bulk prefetch per 1 KB row
+                            prefetch_l2(row, QB * 128u);         // one bulk prefetch per 1 KB row
                         } else {
+                            // the row's own lines only: 656 bytes, or 528 without
+                            // the rope part (line prefetches: one bulk prefetch
+                            // per packed row was slower for E4M3 rows)
+                            if (kp.rope > 0) {
 #pragma unroll
-                            for (uint32_t o = 0; o < kRowBytes; o += 128) prefetch_line_l2(row + o);
-                            prefetch_line_l2(row + kRowBytes - 1);
+                                for (uint32_t o = 0; o < PK_ROW; o += 128) prefetch_line_l2(row + o);
+                                prefetch_line_l2(row + PK_ROW - 1);
+                            } else {
+#pragma unroll
+                                for (uint32_t o = 0; o < PK_ROW - 128; o += 128) prefetch_line_l2(row + o);
+                                prefetch_line_l2(row + PK_ROW - 129);
+                            }
                         }
                     }
                 }
